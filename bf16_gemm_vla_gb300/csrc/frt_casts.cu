@@ -1,0 +1,378 @@
+// Bandwidth kernels: FNUZ -> OCP E4M3 re-encoding and E4M3 quantization.
+//
+// Both dialects put sign, 4 exponent bits and 3 mantissa bits in the same
+// places; FNUZ's exponent bias is one larger, so a byte means half its OCP
+// value, FNUZ has no -0 and its only NaN is 0x80 ("Real-time VLA inference
+// on AMD hardware", "Different FP8 representation"; "Deploying
+// DeepSeek-V4-Flash on AMD MI300X", "The FP8 dialect problem").
+#include <cuda_bf16.h>
+
+#include "frt_host.h"
+
+namespace frt {
+namespace {
+
+// ------------------------------------------------------------------ FNUZ -> OCP
+//
+// Four bytes at a time in a 32-bit word (SIMD within a register).  Per byte,
+// with magnitude g = b & 0x7f:
+//   g >= 0x10 (exponent field >= 2): exponent field - 1, i.e. g - 8;
+//   g <  0x10: value v * 2^-10 with v = g, on the OCP subnormal grid at v / 2:
+//              (v >> 1) + ((v & 1) & ((v >> 1) & 1))  (round half to even);
+//   sign kept (a negative tie to zero becomes 0x80); 0x80 (NaN) -> 0x7f.
+// No byte's arithmetic carries into its neighbour: every intermediate below
+// stays inside its byte lane.
+__device__ __forceinline__ uint32_t fnuz_to_ocp_x4(uint32_t x) {
+  const uint32_t sign = x & 0x80808080u;
+  const uint32_t g = x & 0x7F7F7F7Fu;
+  // high bit of each lane set where g >= 0x10 (g + 0x70 <= 0xef, no carry out)
+  const uint32_t big_hi = (g + 0x70707070u) & 0x80808080u;
+  const uint32_t big = (big_hi >> 7) * 0xFFu;  // 0xff lanes where g >= 0x10
+  // g - 8 with a borrow guard bit in every lane
+  const uint32_t dec = ((g | 0x80808080u) - 0x08080808u) & 0x7F7F7F7Fu;
+  // small magnitudes: h = g >> 1 (3 bits), + 1 when g is odd and h is odd
+  const uint32_t h = (g >> 1) & 0x07070707u;
+  const uint32_t small = h + (g & h & 0x01010101u);
+  uint32_t out = ((big & dec) | (~big & small)) | sign;
+  // lanes that were exactly 0x80: g == 0 and sign set -> 0x7f
+  const uint32_t zero_hi = ~(g + 0x7F7F7F7Fu) & 0x80808080u;
+  const uint32_t nan_hi = zero_hi & sign;
+  out ^= (nan_hi >> 7) * 0xFFu;  // 0x80 ^ 0xff = 0x7f
+  return out;
+}
+
+__global__ void fnuz_to_ocp_vec_kernel(const uint4* __restrict__ in, uint4* __restrict__ out,
+                                       size_t n16) {
+  const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
+  for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n16;
+       i += stride) {
+    uint4 v = in[i];
+    v.x = fnuz_to_ocp_x4(v.x);
+    v.y = fnuz_to_ocp_x4(v.y);
+    v.z = fnuz_to_ocp_x4(v.z);
+    v.w = fnuz_to_ocp_x4(v.w);
+    out[i] = v;
+  }
+}
+
+__global__ void fnuz_to_ocp_byte_kernel(const uint8_t* in, uint8_t* out, size_t n) {
+  const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
+  for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride)
+    out[i] = static_cast<uint8_t>(fnuz_to_ocp_x4(in[i]) & 0xFFu);
+}
+
+// ------------------------------------------------------------------ E4M3 encode
+//
+// Round-to-nearest-even with saturation on the fp32 bit pattern.  For a
+// magnitude a below the dialect's maximum:
+//   a below the smallest normal 2^emin: the codes are spaced 2^(emin-3), so
+//     the code is a * 2^(3-emin) rounded half-to-even (an exact power-of-two
+//     scaling followed by an integer rounding; 8 lands on the smallest normal);
+//   otherwise: keep 3 of the 23 mantissa bits, rounding half to even by
+//     adding 0x7ffff plus the lowest kept bit (a carry steps into the next
+//     binade), then re-bias the exponent from 127 to the dialect's bias.
+// NaN -> the NaN code; a >= max (inf included) -> +-max; a negative value
+// that rounds to zero keeps its sign in OCP (0x80) and is 0x00 in FNUZ.
+template <bool kFnuz>
+__device__ __forceinline__ uint32_t encode_e4m3(float v) {
+  constexpr int kBias = kFnuz ? 8 : 7;
+  constexpr float kMax = kFnuz ? 240.0f : 448.0f;
+  constexpr uint32_t kMaxCode = kFnuz ? 0x7Fu : 0x7Eu;
+  constexpr uint32_t kNanCode = kFnuz ? 0x80u : 0x7Fu;
+  constexpr float kMinNormal = kFnuz ? 0.0078125f : 0.015625f;  // 2^(1 - bias)
+  constexpr float kSubScale = kFnuz ? 1024.0f : 512.0f;         // 2^(3 - (1 - bias))
+  const uint32_t u = __float_as_uint(v);
+  const uint32_t sign = (u >> 24) & 0x80u;
+  const float a = fabsf(v);
+  if (!(a == a)) return kNanCode;
+  if (a >= kMax) return sign | kMaxCode;
+  uint32_t mag;
+  if (a < kMinNormal) {
+    mag = static_cast<uint32_t>(__float2int_rn(a * kSubScale));
+  } else {
+    const uint32_t ua = __float_as_uint(a);
+    const uint32_t r = (ua + 0x7FFFFu + ((ua >> 20) & 1u)) >> 20;
+    mag = r - static_cast<uint32_t>((127 - kBias) << 3);
+  }
+  if (kFnuz && mag == 0u) return 0u;
+  return sign | mag;
+}
+
+// ------------------------------------------------------------------ quantize
+
+constexpr int kQThreads = 256;
+constexpr int kMaxPartials = 1024;  // per-tensor amax partials (one per block)
+constexpr int kColRowsPerBlock = 64;
+
+template <typename T>
+__device__ __forceinline__ float to_f32(T v);
+template <>
+__device__ __forceinline__ float to_f32<float>(float v) { return v; }
+template <>
+__device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 v) {
+  return __bfloat162float(v);
+}
+
+// 8 consecutive elements of a row (16-byte aligned for bf16, 32 for fp32).
+template <typename T>
+__device__ __forceinline__ void load8(const T* p, float (&f)[8]);
+template <>
+__device__ __forceinline__ void load8<__nv_bfloat16>(const __nv_bfloat16* p, float (&f)[8]) {
+  const uint4 v = __ldg(reinterpret_cast<const uint4*>(p));
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+template <>
+__device__ __forceinline__ void load8<float>(const float* p, float (&f)[8]) {
+  const float4 a = __ldg(reinterpret_cast<const float4*>(p));
+  const float4 b = __ldg(reinterpret_cast<const float4*>(p) + 1);
+  f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+  f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+}
+
+__device__ __forceinline__ float block_max(float v, float* red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    v = threadIdx.x < blockDim.x / 32 ? red[threadIdx.x] : 0.0f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  }
+  return v;  // valid in thread 0
+}
+
+// Per-tensor pass 1: each block's max |x| (NaN ignored by fmaxf) -> partial[block].
+// Vector path: VEC = 8 elements per step; scalar path: VEC = 1.
+template <typename T, int VEC>
+__global__ void __launch_bounds__(kQThreads) amax_tensor_kernel(const T* __restrict__ x,
+                                                               int64_t rows, int64_t cols,
+                                                               int64_t ldx,
+                                                               float* __restrict__ partial) {
+  __shared__ float red[32];
+  float m = 0.0f;
+  const int64_t vpr = cols / VEC;  // vectors per row
+  const int64_t total = rows * vpr;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  const bool dense = ldx == cols;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += stride) {
+    int64_t off = i * VEC;
+    if (!dense) {
+      const int64_t r = i / vpr;
+      off = r * ldx + (i - r * vpr) * VEC;
+    }
+    if constexpr (VEC == 8) {
+      float f[8];
+      load8<T>(x + off, f);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) m = fmaxf(m, fabsf(f[e]));
+    } else {
+      m = fmaxf(m, fabsf(to_f32<T>(x[off])));
+    }
+  }
+  m = block_max(m, red);
+  if (threadIdx.x == 0) partial[blockIdx.x] = m;
+}
+
+// Per-tensor pass 2: reduce the partials to amax, s = amax / max (1 if amax
+// is 0) or the static scale, then q = E4M3(x / s).
+template <typename T, int VEC, bool kFnuz>
+__global__ void __launch_bounds__(kQThreads) encode_tensor_kernel(
+    const T* __restrict__ x, int64_t rows, int64_t cols, int64_t ldx,
+    const float* __restrict__ partial, int npartial, const float* __restrict__ static_scale,
+    uint8_t* __restrict__ q, float* __restrict__ scale_out) {
+  __shared__ float red[32];
+  __shared__ float s_sh;
+  if (static_scale) {
+    if (threadIdx.x == 0) s_sh = __ldg(static_scale);
+  } else {
+    float m = 0.0f;
+    for (int i = threadIdx.x; i < npartial; i += blockDim.x) m = fmaxf(m, partial[i]);
+    m = block_max(m, red);
+    if (threadIdx.x == 0) s_sh = m == 0.0f ? 1.0f : __fdiv_rn(m, kFnuz ? 240.0f : 448.0f);
+  }
+  __syncthreads();
+  const float s = s_sh;
+  if (blockIdx.x == 0 && threadIdx.x == 0 && scale_out) *scale_out = s;
+  const int64_t vpr = cols / VEC;
+  const int64_t total = rows * vpr;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  const bool dense = ldx == cols;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += stride) {
+    int64_t off = i * VEC;  // q is dense: element (r, c) at r * cols + c = i * VEC
+    int64_t xoff = off;
+    if (!dense) {
+      const int64_t r = i / vpr;
+      xoff = r * ldx + (i - r * vpr) * VEC;
+    }
+    if constexpr (VEC == 8) {
+      float f[8];
+      load8<T>(x + xoff, f);
+      uint32_t lo = 0, hi = 0;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) lo |= encode_e4m3<kFnuz>(__fdiv_rn(f[e], s)) << (8 * e);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) hi |= encode_e4m3<kFnuz>(__fdiv_rn(f[4 + e], s)) << (8 * e);
+      *reinterpret_cast<uint2*>(q + off) = make_uint2(lo, hi);
+    } else {
+      q[off] = static_cast<uint8_t>(encode_e4m3<kFnuz>(__fdiv_rn(to_f32<T>(x[xoff]), s)));
+    }
+  }
+}
+
+// Per-column pass 1: block (bx, by) covers columns [bx*256, +256) and rows
+// [by*kColRowsPerBlock, +kColRowsPerBlock); partial[by * cols + c] = max |x|.
+template <typename T>
+__global__ void __launch_bounds__(kQThreads) amax_col_kernel(const T* __restrict__ x,
+                                                            int64_t rows, int64_t cols,
+                                                            int64_t ldx,
+                                                            float* __restrict__ partial) {
+  const int64_t c = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (c >= cols) return;
+  const int64_t r0 = static_cast<int64_t>(blockIdx.y) * kColRowsPerBlock;
+  const int64_t r1 = min(rows, r0 + kColRowsPerBlock);
+  float m = 0.0f;
+  for (int64_t r = r0; r < r1; ++r) m = fmaxf(m, fabsf(to_f32<T>(x[r * ldx + c])));
+  partial[static_cast<int64_t>(blockIdx.y) * cols + c] = m;
+}
+
+// Per-column pass 2: s[c] from the partials of column c (or the static
+// scales), then q = E4M3(x / s[c]) for this block's rows.
+template <typename T, bool kFnuz>
+__global__ void __launch_bounds__(kQThreads) encode_col_kernel(
+    const T* __restrict__ x, int64_t rows, int64_t cols, int64_t ldx,
+    const float* __restrict__ partial, int npartial, const float* __restrict__ static_scale,
+    uint8_t* __restrict__ q, float* __restrict__ scale_out) {
+  const int64_t c = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (c >= cols) return;
+  float s;
+  if (static_scale) {
+    s = __ldg(static_scale + c);
+  } else {
+    float m = 0.0f;
+    for (int i = 0; i < npartial; ++i) m = fmaxf(m, partial[static_cast<int64_t>(i) * cols + c]);
+    s = m == 0.0f ? 1.0f : __fdiv_rn(m, kFnuz ? 240.0f : 448.0f);
+  }
+  if (blockIdx.y == 0 && scale_out) scale_out[c] = s;
+  const int64_t r0 = static_cast<int64_t>(blockIdx.y) * kColRowsPerBlock;
+  const int64_t r1 = min(rows, r0 + kColRowsPerBlock);
+  for (int64_t r = r0; r < r1; ++r)
+    q[r * cols + c] = static_cast<uint8_t>(encode_e4m3<kFnuz>(__fdiv_rn(to_f32<T>(x[r * ldx + c]), s)));
+}
+
+int tensor_grid(int64_t total_vecs) {
+  const int64_t want = ceil_div(total_vecs, kQThreads);
+  const int64_t cap = static_cast<int64_t>(sm_count() > 0 ? sm_count() : 148) * 4;
+  int64_t g = want < cap ? want : cap;
+  if (g > kMaxPartials) g = kMaxPartials;
+  return static_cast<int>(g < 1 ? 1 : g);
+}
+
+template <typename T, bool kFnuz>
+frt_status quantize_typed(const T* x, int64_t rows, int64_t cols, int64_t ldx, frt_scale_mode mode,
+                          const float* static_scale, uint8_t* q, float* scale, float* ws,
+                          cudaStream_t st) {
+  if (mode == FRT_SCALE_PER_TENSOR) {
+    const bool vec = aligned(x, 16) && aligned(q, 8) && cols % 8 == 0 && ldx % 8 == 0;
+    const int64_t total = rows * (vec ? cols / 8 : cols);
+    const int grid = tensor_grid(total);
+    if (vec) {
+      if (!static_scale) amax_tensor_kernel<T, 8><<<grid, kQThreads, 0, st>>>(x, rows, cols, ldx, ws);
+      encode_tensor_kernel<T, 8, kFnuz>
+          <<<grid, kQThreads, 0, st>>>(x, rows, cols, ldx, ws, grid, static_scale, q, scale);
+    } else {
+      if (!static_scale) amax_tensor_kernel<T, 1><<<grid, kQThreads, 0, st>>>(x, rows, cols, ldx, ws);
+      encode_tensor_kernel<T, 1, kFnuz>
+          <<<grid, kQThreads, 0, st>>>(x, rows, cols, ldx, ws, grid, static_scale, q, scale);
+    }
+  } else {
+    const dim3 grid(static_cast<unsigned>(ceil_div(cols, kQThreads)),
+                    static_cast<unsigned>(ceil_div(rows, kColRowsPerBlock)));
+    if (!static_scale) amax_col_kernel<T><<<grid, kQThreads, 0, st>>>(x, rows, cols, ldx, ws);
+    encode_col_kernel<T, kFnuz><<<grid, kQThreads, 0, st>>>(x, rows, cols, ldx, ws,
+                                                             static_cast<int>(grid.y),
+                                                             static_scale, q, scale);
+  }
+  return launch_status();
+}
+
+}  // namespace
+}  // namespace frt
+
+extern "C" size_t frt_quantize_workspace_bytes(int64_t rows, int64_t cols, frt_scale_mode mode) {
+  if (rows < 0 || cols < 0) return 0;
+  if (mode == FRT_SCALE_PER_COL)
+    return static_cast<size_t>(frt::ceil_div(rows, frt::kColRowsPerBlock) * cols) * sizeof(float);
+  return static_cast<size_t>(frt::kMaxPartials) * sizeof(float);
+}
+
+extern "C" frt_status frt_quantize_e4m3(const void* x, frt_dtype x_dtype, int64_t rows,
+                                        int64_t cols, int64_t ldx, frt_scale_mode mode,
+                                        frt_dtype out_fmt, const float* static_scale, uint8_t* q,
+                                        float* scale, void* workspace, size_t workspace_bytes,
+                                        frt_stream_t stream) {
+  using namespace frt;
+  if (x_dtype != FRT_BF16 && x_dtype != FRT_F32) return FRT_ERR_INVALID_ARG;
+  if (out_fmt != FRT_E4M3_OCP && out_fmt != FRT_E4M3_FNUZ) return FRT_ERR_INVALID_ARG;
+  if (mode != FRT_SCALE_PER_TENSOR && mode != FRT_SCALE_PER_COL) return FRT_ERR_INVALID_ARG;
+  if (rows < 0 || cols < 0 || ldx < cols) return FRT_ERR_INVALID_ARG;
+  if (rows == 0 || cols == 0) return FRT_OK;
+  if (!x || !q) return FRT_ERR_INVALID_ARG;
+  if (!static_scale && !workspace) return FRT_ERR_INVALID_ARG;
+  if (rows > (1LL << 40) || cols > (1LL << 31)) return FRT_ERR_UNSUPPORTED_SHAPE;
+  const size_t esize = x_dtype == FRT_BF16 ? 2 : 4;
+  if (!aligned(x, esize) || (scale && !aligned(scale, 4)) ||
+      (static_scale && !aligned(static_scale, 4)) || (workspace && !aligned(workspace, 4)))
+    return FRT_ERR_MISALIGNED;
+  if (!static_scale && workspace_bytes < frt_quantize_workspace_bytes(rows, cols, mode))
+    return FRT_ERR_WORKSPACE_TOO_SMALL;
+  float* ws = static_cast<float*>(workspace);
+  cudaStream_t st = as_cuda(stream);
+  const bool fnuz = out_fmt == FRT_E4M3_FNUZ;
+  if (x_dtype == FRT_BF16) {
+    const auto* xb = static_cast<const __nv_bfloat16*>(x);
+    return fnuz ? quantize_typed<__nv_bfloat16, true>(xb, rows, cols, ldx, mode, static_scale, q,
+                                                      scale, ws, st)
+                : quantize_typed<__nv_bfloat16, false>(xb, rows, cols, ldx, mode, static_scale,
+                                                       q, scale, ws, st);
+  }
+  const auto* xf = static_cast<const float*>(x);
+  return fnuz ? quantize_typed<float, true>(xf, rows, cols, ldx, mode, static_scale, q, scale, ws,
+                                            st)
+              : quantize_typed<float, false>(xf, rows, cols, ldx, mode, static_scale, q, scale,
+                                             ws, st);
+}
+
+extern "C" frt_status frt_fnuz_to_ocp(const uint8_t* in, uint8_t* out, size_t n,
+                                      frt_stream_t stream) {
+  using namespace frt;
+  if (n == 0) return FRT_OK;
+  if (!in || !out) return FRT_ERR_INVALID_ARG;
+  const uintptr_t a = reinterpret_cast<uintptr_t>(in), b = reinterpret_cast<uintptr_t>(out);
+  if (a != b && a < b + n && b < a + n) return FRT_ERR_INVALID_ARG;  // partial overlap
+  cudaStream_t st = as_cuda(stream);
+  const int cap = (sm_count() > 0 ? sm_count() : 148) * 8;
+  if (aligned(in, 16) && aligned(out, 16)) {
+    const size_t n16 = n / 16;
+    if (n16) {
+      const int64_t want = ceil_div(static_cast<int64_t>(n16), 256);
+      const int grid = static_cast<int>(want < cap ? want : cap);
+      fnuz_to_ocp_vec_kernel<<<grid, 256, 0, st>>>(reinterpret_cast<const uint4*>(in),
+                                                   reinterpret_cast<uint4*>(out), n16);
+    }
+    const size_t tail = n - n16 * 16;
+    if (tail) fnuz_to_ocp_byte_kernel<<<1, 32, 0, st>>>(in + n16 * 16, out + n16 * 16, tail);
+  } else {
+    const int64_t want = ceil_div(static_cast<int64_t>(n), 256);
+    const int grid = static_cast<int>(want < cap ? want : cap);
+    fnuz_to_ocp_byte_kernel<<<grid, 256, 0, st>>>(in, out, n);
+  }
+  return launch_status();
+}

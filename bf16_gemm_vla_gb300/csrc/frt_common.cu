@@ -1,0 +1,37 @@
+// Status strings, ABI version and device queries.
+#include <mutex>
+
+#include "frt_host.h"
+
+namespace frt {
+
+int sm_count() {
+  static std::mutex mu;
+  static int counts[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if (counts[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess)
+      counts[dev] = n;
+  }
+  return counts[dev];
+}
+
+}  // namespace frt
+
+extern "C" int frt_abi_version(void) { return 1; }
+
+extern "C" const char* frt_status_string(frt_status s) {
+  switch (s) {
+    case FRT_OK: return "FRT_OK";
+    case FRT_ERR_INVALID_ARG: return "FRT_ERR_INVALID_ARG";
+    case FRT_ERR_UNSUPPORTED_SHAPE: return "FRT_ERR_UNSUPPORTED_SHAPE";
+    case FRT_ERR_MISALIGNED: return "FRT_ERR_MISALIGNED";
+    case FRT_ERR_WORKSPACE_TOO_SMALL: return "FRT_ERR_WORKSPACE_TOO_SMALL";
+    case FRT_ERR_CUDA: return "FRT_ERR_CUDA";
+    case FRT_ERR_TIMEOUT: return "FRT_ERR_TIMEOUT";
+  }
+  return "FRT_ERR_UNKNOWN";
+}

@@ -1,0 +1,177 @@
+"""Python binding of libfrt: the same entry points as include/frt.h, taking
+torch tensors.  Argument marshalling only -- every step of the path runs in
+the library's CUDA kernels; PyTorch provides device memory and the stream.
+
+Outputs that are not passed in are allocated with torch; for CUDA-graph
+capture pass every buffer in (the calls then allocate nothing).
+"""
+import torch
+
+from . import _lib
+
+OCP = "ocp"
+FNUZ = "fnuz"
+PER_TENSOR = "per_tensor"
+PER_COL = "per_col"
+
+_FMT = {OCP: _lib.FRT_E4M3_OCP, FNUZ: _lib.FRT_E4M3_FNUZ}
+_MODE = {PER_TENSOR: _lib.FRT_SCALE_PER_TENSOR, PER_COL: _lib.FRT_SCALE_PER_COL}
+_XDT = {torch.bfloat16: _lib.FRT_BF16, torch.float32: _lib.FRT_F32}
+
+
+class FrtError(RuntimeError):
+    """A libfrt call returned a status other than FRT_OK."""
+
+    def __init__(self, fn, status):
+        self.status = status
+        super().__init__("%s failed: %s" % (fn, _lib.STATUS_NAMES.get(status, status)))
+
+
+def _check(fn, status):
+    if status != _lib.FRT_OK:
+        raise FrtError(fn, status)
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def lib():
+    return _lib.load()
+
+
+def _rows_view(x, name):
+    if x.dim() != 2 or (x.shape[1] > 1 and x.stride(1) != 1) or not x.is_cuda:
+        raise ValueError("%s must be a 2-D CUDA tensor with unit column stride" % name)
+    return x.shape[0], x.shape[1], x.stride(0)
+
+
+# ---------------------------------------------------------------- quantize
+
+def frt_quantize_workspace_bytes(rows, cols, mode=PER_TENSOR):
+    return lib().frt_quantize_workspace_bytes(rows, cols, _MODE[mode])
+
+
+def frt_quantize_e4m3(x, mode=PER_TENSOR, out_fmt=OCP, static_scale=None, q=None, scale=None,
+                      workspace=None, stream=None):
+    """E4M3 bytes and dequant scale(s) of a 2-D bf16/fp32 tensor (rows may be
+    strided).  Returns (q uint8 [rows x cols], scale fp32 [1] or [cols])."""
+    rows, cols, ldx = _rows_view(x, "x")
+    L = lib()
+    if q is None:
+        q = torch.empty((rows, cols), dtype=torch.uint8, device=x.device)
+    if scale is None:
+        scale = torch.empty((cols if mode == PER_COL else 1,), dtype=torch.float32, device=x.device)
+    if static_scale is None and workspace is None:
+        nb = L.frt_quantize_workspace_bytes(rows, cols, _MODE[mode])
+        workspace = torch.empty((max(nb, 4) // 4,), dtype=torch.float32, device=x.device)
+    wsb = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("frt_quantize_e4m3",
+           L.frt_quantize_e4m3(x.data_ptr(), _XDT[x.dtype], rows, cols, ldx, _MODE[mode],
+                               _FMT[out_fmt], _ptr(static_scale), q.data_ptr(), _ptr(scale),
+                               _ptr(workspace), wsb, _stream(stream)))
+    return q, scale
+
+
+# ---------------------------------------------------------------- FNUZ -> OCP
+
+def frt_fnuz_to_ocp(inp, out=None, stream=None):
+    """OCP bytes holding the values of FNUZ bytes (out may be inp)."""
+    if inp.dtype != torch.uint8 or not inp.is_contiguous():
+        raise ValueError("inp must be a contiguous uint8 tensor")
+    if out is None:
+        out = torch.empty_like(inp)
+    _check("frt_fnuz_to_ocp",
+           lib().frt_fnuz_to_ocp(inp.data_ptr(), out.data_ptr(), inp.numel(), _stream(stream)))
+    return out
+
+
+# ---------------------------------------------------------------- pack
+
+def frt_packed_weight_bytes(K, N, packed_dtype="e4m3"):
+    dt = _lib.FRT_E4M3_OCP if packed_dtype == "e4m3" else _lib.FRT_BF16
+    return lib().frt_packed_weight_bytes(K, N, dt)
+
+
+def frt_pack_weights(w, packed_dtype="e4m3", packed=None, stream=None):
+    """Packs W [K x N] (uint8 OCP E4M3 bytes for 'e4m3'; fp32 or bf16 for
+    'bf16') into the kernels' tile layout; returns the uint8 buffer."""
+    K, N, ldw = _rows_view(w, "w")
+    if packed_dtype == "e4m3":
+        if w.dtype != torch.uint8:
+            raise ValueError("e4m3 packing takes OCP E4M3 bytes (uint8)")
+        wdt, pdt = _lib.FRT_E4M3_OCP, _lib.FRT_E4M3_OCP
+    else:
+        wdt, pdt = _XDT[w.dtype], _lib.FRT_BF16
+    nbytes = lib().frt_packed_weight_bytes(K, N, pdt)
+    if packed is None:
+        packed = torch.empty((nbytes,), dtype=torch.uint8, device=w.device)
+    _check("frt_pack_weights",
+           lib().frt_pack_weights(w.data_ptr(), wdt, K, N, ldw, pdt, packed.data_ptr(),
+                                  packed.numel(), _stream(stream)))
+    return packed
+
+
+# ---------------------------------------------------------------- GEMMs
+
+_STATUS = {}
+
+
+def device_status(device=None):
+    """The per-device int32 status word the GEMMs report bounded-wait
+    expiry into (zero while healthy)."""
+    dev = torch.device("cuda", torch.cuda.current_device() if device is None else device.index)
+    if dev not in _STATUS:
+        _STATUS[dev] = torch.zeros((1,), dtype=torch.int32, device=dev)
+    return _STATUS[dev]
+
+
+def check_device_status(device=None):
+    """Raises FrtError(FRT_ERR_TIMEOUT) if a kernel reported an expired wait
+    (synchronises with the device)."""
+    st = device_status(device)
+    code = int(st.item())
+    if code:
+        st.zero_()
+        raise FrtError("device wait (code 0x%x)" % code, 6)
+
+
+def _gemm_out(M, N, out, device):
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=device)
+    if out.dtype != torch.bfloat16:
+        raise ValueError("out must be bf16")
+    _, _, ldo = _rows_view(out, "out")
+    return out, ldo
+
+
+def frt_gemm_fp8(a_q, a_scale, w_packed, w_scale, N, bias=None, act_cols=0, out=None,
+                 stream=None):
+    """out = bf16(act(a_scale * w_scale[n] * (A_q . W) + bias[n])), GELU on
+    the first act_cols columns.  a_q: [M x K] OCP E4M3 bytes."""
+    M, K, lda = _rows_view(a_q, "a_q")
+    out, ldo = _gemm_out(M, N, out, a_q.device)
+    act = _lib.FRT_ACT_GELU_TANH if act_cols else _lib.FRT_ACT_NONE
+    _check("frt_gemm_fp8",
+           lib().frt_gemm_fp8(a_q.data_ptr(), lda, _ptr(a_scale), w_packed.data_ptr(),
+                              _ptr(w_scale), _ptr(bias), M, N, K, act, act_cols, out.data_ptr(),
+                              ldo, None, 0, device_status(a_q.device).data_ptr(),
+                              _stream(stream)))
+    return out
+
+
+def frt_gemm_bf16(a, w_packed, N, w_scale=None, bias=None, act_cols=0, out=None, stream=None):
+    """out = bf16(act(w_scale[n] * (A . W) + bias[n])).  a: [M x K] bf16."""
+    M, K, lda = _rows_view(a, "a")
+    out, ldo = _gemm_out(M, N, out, a.device)
+    act = _lib.FRT_ACT_GELU_TANH if act_cols else _lib.FRT_ACT_NONE
+    _check("frt_gemm_bf16",
+           lib().frt_gemm_bf16(a.data_ptr(), lda, w_packed.data_ptr(), _ptr(w_scale), _ptr(bias),
+                               M, N, K, act, act_cols, out.data_ptr(), ldo, None, 0,
+                               device_status(a.device).data_ptr(), _stream(stream)))
+    return out

@@ -1,0 +1,83 @@
+"""Load-time weight preparation and a static-buffer linear layer.
+
+Load time ("Real-time VLA inference on AMD hardware", "How FlashRT works":
+the weights are quantized and packed once, at load, and the choices are
+frozen before the graph is recorded):
+
+  FP8:  W fp32 [K x N] --quantize per output channel--> E4M3 bytes + scales
+        (optionally produced in FNUZ, as an import from a CDNA3 checkpoint,
+        then re-encoded to OCP) --pack--> tile layout.
+  BF16: W fp32 --round to bf16 and pack--> tile layout.
+
+A ``Linear`` owns every buffer its forward touches (the quantized
+activation, its scale, the quantize workspace and the output), so a
+sequence of ``Linear`` calls can be captured into a CUDA graph and replayed
+with static pointers and shapes.
+"""
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+from . import frt
+
+
+@dataclass
+class PackedWeight:
+    packed: torch.Tensor            # uint8 tile-layout buffer
+    K: int
+    N: int
+    kind: str                       # "e4m3" or "bf16"
+    w_scale: Optional[torch.Tensor]  # fp32 [N] (FP8) or None
+    bias: Optional[torch.Tensor]    # fp32 [N] or None
+
+
+def prepare_fp8(w_f32, bias=None, import_fnuz=False):
+    """Quantize W per output channel to E4M3 and pack it.  With
+    ``import_fnuz`` the bytes are first produced in FNUZ (scale amax/240)
+    and re-encoded to OCP in place."""
+    K, N = w_f32.shape
+    fmt = frt.FNUZ if import_fnuz else frt.OCP
+    q, s = frt.frt_quantize_e4m3(w_f32, frt.PER_COL, fmt)
+    if import_fnuz:
+        frt.frt_fnuz_to_ocp(q.view(-1), out=q.view(-1))
+    packed = frt.frt_pack_weights(q, "e4m3")
+    return PackedWeight(packed, K, N, "e4m3", s, bias)
+
+
+def prepare_bf16(w, bias=None):
+    """Round W (fp32 or bf16) to bf16 and pack it."""
+    K, N = w.shape
+    return PackedWeight(frt.frt_pack_weights(w, "bf16"), K, N, "bf16", None, bias)
+
+
+class Linear:
+    """One linear layer with static buffers, for a fixed number of rows M.
+
+    FP8:  q, s = quantize(x) per tensor (OCP); out = gemm_fp8(q, s, W).
+    BF16: out = gemm_bf16(x, W).
+    ``act_cols`` output columns get the tanh-GELU.
+    """
+
+    def __init__(self, weight: PackedWeight, M, act_cols=0, out=None, device=None):
+        self.w = weight
+        self.M = M
+        self.act_cols = act_cols
+        dev = device if device is not None else weight.packed.device
+        self.out = out if out is not None else torch.empty((M, weight.N), dtype=torch.bfloat16,
+                                                            device=dev)
+        if weight.kind == "e4m3":
+            self.q = torch.empty((M, weight.K), dtype=torch.uint8, device=dev)
+            self.a_scale = torch.empty((1,), dtype=torch.float32, device=dev)
+            nb = frt.frt_quantize_workspace_bytes(M, weight.K, frt.PER_TENSOR)
+            self.ws = torch.empty((max(nb, 4) // 4,), dtype=torch.float32, device=dev)
+
+    def __call__(self, x, stream=None):
+        w = self.w
+        if w.kind == "e4m3":
+            frt.frt_quantize_e4m3(x, frt.PER_TENSOR, frt.OCP, q=self.q, scale=self.a_scale,
+                                  workspace=self.ws, stream=stream)
+            return frt.frt_gemm_fp8(self.q, self.a_scale, w.packed, w.w_scale, w.N, bias=w.bias,
+                                    act_cols=self.act_cols, out=self.out, stream=stream)
+        return frt.frt_gemm_bf16(x, w.packed, w.N, w_scale=w.w_scale, bias=w.bias,
+                                 act_cols=self.act_cols, out=self.out, stream=stream)

@@ -1,0 +1,121 @@
+"""The synthetic encoder/decoder stack, captured and replayed as one CUDA graph.
+
+The method records the whole forward once and replays it, so the per-op
+launch overhead is paid once at load ("Real-time VLA inference on AMD
+hardware", "How FlashRT works"; the recorded region must use static
+pointers, no allocation and no host reads, "Deploying DeepSeek-V4-Flash on
+AMD MI300X", "HIP Graphs").  The stack here is the linear-layer skeleton of
+a pi0.5-style pass:
+
+  encoder: 18 layers at M = 768, hidden 2048, FP8 -- QKV 2048->2560,
+           O 2048->2048, merged gate/up 2048->2x16384 (tanh-GELU on the gate
+           half), down 16384->2048; every GEMM preceded by a per-tensor
+           activation quantize;
+  decoder: 18 layers at M = 50, hidden 1024, BF16 -- QKV 1024->2560,
+           O 2048->1024, gate/up 1024->2x4096, down 4096->1024.
+
+Attention, the GeGLU product, residuals and norms are not part of this
+path.  Their places are taken by strided views: O reads the first K columns
+of the QKV output, down reads the gate half of the gate/up output, and the
+next layer reads the down output.
+
+Weights (N(0, 0.02)) and biases (N(0, 0.1)) are drawn on the device from a
+seeded torch generator, one layer after another in the order above.
+"""
+import torch
+
+from . import layers
+
+ENCODER = (("qkv", 2048, 2560, 0), ("o", 2048, 2048, 0), ("gate_up", 2048, 32768, 16384),
+           ("down", 16384, 2048, 0))
+DECODER = (("qkv", 1024, 2560, 0), ("o", 2048, 1024, 0), ("gate_up", 1024, 8192, 4096),
+           ("down", 4096, 1024, 0))
+M_ENC = 768
+M_DEC = 50
+
+
+class SyntheticStack:
+    def __init__(self, n_layers=18, seed=1, device="cuda", enc_kind="e4m3", dec_kind="bf16",
+                 keep=(0, 17)):
+        self.device = torch.device(device)
+        self.n_layers = n_layers
+        g = torch.Generator(device=self.device)
+        g.manual_seed(seed)
+        self.kept = {}  # (part, layer, name) -> (w fp32 cpu, bias fp32 cpu)
+        self.enc = self._build("enc", ENCODER, M_ENC, enc_kind, g, keep)
+        self.dec = self._build("dec", DECODER, M_DEC, dec_kind, g, keep)
+        self.x_enc = torch.zeros((M_ENC, ENCODER[0][1]), dtype=torch.bfloat16, device=self.device)
+        self.x_dec = torch.zeros((M_DEC, DECODER[0][1]), dtype=torch.bfloat16, device=self.device)
+        self.graph = None
+
+    def _build(self, part, spec, M, kind, g, keep):
+        out = []
+        for li in range(self.n_layers):
+            lay = {}
+            for name, K, N, act in spec:
+                w = torch.randn((K, N), generator=g, device=self.device, dtype=torch.float32) * 0.02
+                b = torch.randn((N,), generator=g, device=self.device, dtype=torch.float32) * 0.1
+                if li in keep:
+                    self.kept[(part, li, name)] = (w.cpu(), b.cpu())
+                pw = layers.prepare_fp8(w, b) if kind == "e4m3" else layers.prepare_bf16(w, b)
+                lay[name] = layers.Linear(pw, M, act_cols=act, device=self.device)
+                del w
+            out.append(lay)
+        return out
+
+    @staticmethod
+    def _run_chain(chain, x, stream):
+        for lay in chain:
+            qkv = lay["qkv"](x, stream)
+            o = lay["o"](qkv[:, : lay["o"].w.K], stream)
+            gu = lay["gate_up"](o, stream)
+            x = lay["down"](gu[:, : lay["down"].w.K], stream)
+        return x
+
+    def inputs_of(self, part, li, name):
+        """The activation tensor layer (part, li, name) reads, after a forward."""
+        chain = self.enc if part == "enc" else self.dec
+        lay = chain[li]
+        if name == "qkv":
+            if li == 0:
+                return self.x_enc if part == "enc" else self.x_dec
+            return chain[li - 1]["down"].out
+        if name == "o":
+            return lay["qkv"].out[:, : lay["o"].w.K]
+        if name == "gate_up":
+            return lay["o"].out
+        return lay["gate_up"].out[:, : lay["down"].w.K]
+
+    def forward(self, stream=None):
+        """One eager pass (encoder chain, then decoder chain)."""
+        e = self._run_chain(self.enc, self.x_enc, stream)
+        d = self._run_chain(self.dec, self.x_dec, stream)
+        return e, d
+
+    def launches_per_forward(self):
+        n = 0
+        for chain in (self.enc, self.dec):
+            for lay in chain:
+                for lin in lay.values():
+                    n += 3 if lin.w.kind == "e4m3" else 1  # amax + encode + GEMM
+        return n
+
+    def capture(self):
+        """Records one forward into a CUDA graph (after one eager warm-up that
+        sets every kernel's attributes)."""
+        s = torch.cuda.Stream(device=self.device)
+        s.wait_stream(torch.cuda.current_stream(self.device))
+        with torch.cuda.stream(s):
+            self.forward()
+        torch.cuda.current_stream(self.device).wait_stream(s)
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            self.forward()
+        return self.graph
+
+    def replay(self):
+        self.graph.replay()
+
+    def weight_bytes(self):
+        return sum(lin.w.packed.numel() for chain in (self.enc, self.dec)
+                   for lay in chain for lin in lay.values())

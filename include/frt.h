@@ -1,0 +1,211 @@
+/*
+ * frt.h -- C ABI of libfrt: the quantized linear layers of a small-batch,
+ * latency-bound VLA forward pass on GB300 (sm_103a).
+ *
+ * The path (sources cited by page title and section):
+ *   - E4M3 activation quantization: amax, fp32 scale, round-to-nearest-even
+ *     with saturation ("Real-time VLA inference on AMD hardware", "How
+ *     FlashRT works": weights and activations are quantized to FP8);
+ *   - FNUZ -> OCP re-encoding of imported E4M3 bytes: same bit layout,
+ *     exponent bias off by one, a byte read in the wrong dialect is 2x off
+ *     (same page, "Different FP8 representation"; "Deploying
+ *     DeepSeek-V4-Flash on AMD MI300X", "The FP8 dialect problem");
+ *   - load-time weight packing into the layout the tensor-core kernels read,
+ *     at a fixed address for graph replay (first page, "Packing around the
+ *     instruction");
+ *   - FP8 and BF16 GEMMs, fp32 accumulation, with the per-channel scale,
+ *     bias and optional tanh-GELU applied in the epilogue and a bf16 store
+ *     (first page, "Merging gate and up": the bias is applied in the GEMM
+ *     epilogue; a merged [W_gate, W_up] weight is one GEMM).
+ *
+ * Conventions shared by every entry point:
+ *   - Pointers named x, q, w, packed, a, out, scale, bias, workspace and
+ *     dev_status are DEVICE pointers; the caller owns every buffer.  The
+ *     library never allocates or frees device memory and never synchronises
+ *     the stream; work is enqueued on `stream` (NULL = the legacy default
+ *     stream), so every call is legal inside CUDA stream capture and can be
+ *     replayed from a CUDA graph with the same pointers and shapes.
+ *   - Shapes and leading dimensions are in ELEMENTS.  Matrices are row-major.
+ *   - Arguments are checked on the host before anything is enqueued; a
+ *     failed check returns its status and enqueues nothing.  A launch
+ *     failure returns FRT_ERR_CUDA (from cudaGetLastError).
+ *   - The first call that launches a given kernel sets its function
+ *     attributes (dynamic shared memory size); make one eager call of each
+ *     entry point before capturing a graph.
+ *   - Kernels run only on sm_103a (GB300); on any other device the launch
+ *     fails with FRT_ERR_CUDA.
+ */
+#ifndef FRT_H_
+#define FRT_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ABI-compatible with cudaStream_t / CUstream. */
+typedef struct CUstream_st* frt_stream_t;
+
+typedef enum {
+  FRT_OK = 0,
+  FRT_ERR_INVALID_ARG = 1,         /* null pointer, negative size, bad enum */
+  FRT_ERR_UNSUPPORTED_SHAPE = 2,   /* a size constraint below is not met */
+  FRT_ERR_MISALIGNED = 3,          /* a pointer or leading dimension is not aligned */
+  FRT_ERR_WORKSPACE_TOO_SMALL = 4, /* workspace or packed buffer smaller than required */
+  FRT_ERR_CUDA = 5,                /* a CUDA runtime call or launch failed */
+  FRT_ERR_TIMEOUT = 6              /* a device-side bounded wait expired (see dev_status) */
+} frt_status;
+
+typedef enum {
+  FRT_F32 = 0,
+  FRT_BF16 = 1,
+  FRT_E4M3_OCP = 2,  /* OCP E4M3: bias 7, max 448, NaN = 0x7f/0xff, has -0 */
+  FRT_E4M3_FNUZ = 3  /* FNUZ E4M3: bias 8, max 240, NaN = 0x80 only, no -0 */
+} frt_dtype;
+
+typedef enum {
+  FRT_SCALE_PER_TENSOR = 0, /* one scale for the whole tensor */
+  FRT_SCALE_PER_COL = 1     /* one scale per column c of a [rows x cols] tensor */
+} frt_scale_mode;
+
+typedef enum {
+  FRT_ACT_NONE = 0,
+  FRT_ACT_GELU_TANH = 1 /* 0.5 v (1 + tanh(sqrt(2/pi) (v + 0.044715 v^3))) */
+} frt_act;
+
+/* Version of this ABI (incremented on any signature change). */
+int frt_abi_version(void);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* frt_status_string(frt_status status);
+
+/* ------------------------------------------------------------------------
+ * E4M3 quantization ("Real-time VLA inference on AMD hardware", "How FlashRT
+ * works" and "Different FP8 representation").
+ *
+ *   amax  = max |x| over the tensor (FRT_SCALE_PER_TENSOR) or over the rows
+ *           of each column (FRT_SCALE_PER_COL); NaN elements are ignored.
+ *   s     = amax / max_finite, one IEEE fp32 division (448 for OCP, 240 for
+ *           FNUZ); s = 1 where amax == 0.  s is the DEQUANT multiplier:
+ *           x ~= decode(q) * s.
+ *   q     = E4M3(x / s), the quotient an IEEE fp32 division, encoded with
+ *           round-to-nearest-even and saturation: NaN -> the NaN code (OCP
+ *           0x7f, FNUZ 0x80), |v| >= max_finite (inf included) -> +-max;
+ *           a negative value that rounds to zero is 0x80 in OCP, 0x00 in FNUZ.
+ *
+ * x         : [rows x cols] of x_dtype (FRT_BF16 or FRT_F32), row stride ldx.
+ * out_fmt   : FRT_E4M3_OCP or FRT_E4M3_FNUZ.
+ * static_scale: NULL -> compute amax and s as above.  Non-NULL -> device
+ *           pointer to the scale(s) to use (1 float, or `cols` floats per
+ *           column); amax is skipped and the workspace is not used.
+ * q         : [rows x cols] bytes, contiguous (row stride cols).
+ * scale     : device, receives s (1 float, or `cols` floats); may be NULL.
+ * workspace : device scratch of frt_quantize_workspace_bytes() bytes, 4-byte
+ *             aligned; its contents need no initialisation and are
+ *             overwritten.  Calls that share a workspace must be ordered on
+ *             one stream.
+ * Requires rows, cols >= 0, ldx >= cols; x, q, scale 4-byte aligned.
+ * Vector paths are taken when x/q are 16-byte aligned and cols, ldx are
+ * multiples of 8; other shapes take a scalar path with the same results.
+ * rows * cols == 0 enqueues nothing and returns FRT_OK (scale is not written).
+ * ---------------------------------------------------------------------- */
+size_t frt_quantize_workspace_bytes(int64_t rows, int64_t cols, frt_scale_mode mode);
+
+frt_status frt_quantize_e4m3(const void* x, frt_dtype x_dtype, int64_t rows, int64_t cols,
+                             int64_t ldx, frt_scale_mode mode, frt_dtype out_fmt,
+                             const float* static_scale, uint8_t* q, float* scale,
+                             void* workspace, size_t workspace_bytes, frt_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * FNUZ -> OCP re-encoding of n E4M3 bytes ("Real-time VLA inference on AMD
+ * hardware", "Different FP8 representation").  Each output byte is the OCP
+ * code of the FNUZ byte's value: exponent field e >= 2 keeps sign and
+ * mantissa with field e - 1 (exact); the 15 smallest FNUZ magnitudes land
+ * on the OCP subnormal grid and round half to even (8 of them are ties), a
+ * negative value rounding to zero becomes 0x80; the FNUZ NaN 0x80 -> 0x7f.
+ * in == out (in place) is allowed; otherwise the ranges must not overlap.
+ * n == 0 enqueues nothing.
+ * ---------------------------------------------------------------------- */
+frt_status frt_fnuz_to_ocp(const uint8_t* in, uint8_t* out, size_t n, frt_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Load-time weight packing ("Real-time VLA inference on AMD hardware",
+ * "Packing around the instruction"; merged gate/up = concatenate the
+ * weights along N before packing, "Merging gate and up").
+ *
+ * W is logical [K x N], row-major with row stride ldw (column n = output
+ * channel).  The packed buffer stores W^T in tiles of 128 channels x 128
+ * bytes of K:
+ *   NB = ceil(N / 128), KB = ceil(K * esize / 128)  (esize 1 for E4M3, 2 for bf16)
+ *   tile (nb, kb) at byte offset (nb * KB + kb) * 16384;
+ *   channel r = n - 128 nb owns bytes [r*128, r*128 + 128) of the tile;
+ *   byte j of its 128 K-bytes (element k = kb*128/esize + j/esize,
+ *   little-endian for bf16) sits at ((j / 16) ^ (r % 8)) * 16 + j % 16.
+ *   Padding (n >= N, k >= K) is zero.
+ * A tile copied byte for byte into 1024-byte-aligned shared memory is the
+ * 128-byte-swizzled K-major operand image the tensor cores read.
+ *
+ * w_dtype -> packed_dtype:  FRT_F32 -> FRT_BF16 (round to nearest even),
+ *                           FRT_BF16 -> FRT_BF16 (copy),
+ *                           FRT_E4M3_OCP -> FRT_E4M3_OCP (bytes, copy).
+ * packed must be 16-byte aligned and hold frt_packed_weight_bytes() bytes.
+ * Returns 0 from frt_packed_weight_bytes for an unsupported packed_dtype.
+ * ---------------------------------------------------------------------- */
+size_t frt_packed_weight_bytes(int64_t K, int64_t N, frt_dtype packed_dtype);
+
+frt_status frt_pack_weights(const void* w, frt_dtype w_dtype, int64_t K, int64_t N, int64_t ldw,
+                            frt_dtype packed_dtype, void* packed, size_t packed_bytes,
+                            frt_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * GEMMs with the fused epilogue ("Real-time VLA inference on AMD hardware",
+ * "FP8 helps the encoder and hurts the decoder" and "Merging gate and up").
+ *
+ *   acc[m, n] = sum_k a[m, k] * w[k, n]            (fp32 accumulation)
+ *   v         = acc * (a_scale * w_scale[n]) + bias[n]
+ *   v         = gelu_tanh(v)   if act == FRT_ACT_GELU_TANH and n < act_cols
+ *   out[m, n] = bf16(v)        (round to nearest even)
+ *
+ * a_q / a   : [M x K] row-major, row stride lda; E4M3 OCP bytes (FP8) or
+ *             bf16 (BF16); 16-byte aligned, lda * esize a multiple of 16.
+ * a_scale   : device, 1 float (the activation's per-tensor dequant scale).
+ * w_packed  : from frt_pack_weights with the same K and N (FRT_E4M3_OCP for
+ *             frt_gemm_fp8, FRT_BF16 for frt_gemm_bf16); 16-byte aligned.
+ * w_scale   : device, N floats (per output channel); NULL means 1.
+ *             Required (non-NULL) for frt_gemm_fp8.
+ * bias      : device, N floats; NULL means 0.
+ * out       : bf16 [M x N], row stride ldo; 16-byte aligned, ldo a multiple of 8.
+ * act_cols  : number of leading output columns the activation applies to
+ *             (0 <= act_cols <= N; a merged gate/up GEMM passes N/2).
+ * workspace : reserved; frt_gemm_workspace_bytes() returns 0 and the
+ *             pointer may be NULL.  (Split-K partial sums are reduced across
+ *             the CTAs of a thread-block cluster in shared memory, in a fixed
+ *             order, so results are deterministic.)
+ * dev_status: optional device int.  Every wait inside the kernels is
+ *             bounded (about one second); if one expires the kernel writes a
+ *             nonzero code there (the first writer wins), abandons its tile
+ *             and exits.  The caller reads it after synchronising; nonzero
+ *             means the output is invalid.  The caller zeroes it once.
+ * Requires M, N, K >= 1; N % 16 == 0; K % 32 == 0 (FP8) or K % 16 == 0
+ * (BF16).  Any M works (row tails are masked).
+ * ---------------------------------------------------------------------- */
+size_t frt_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, frt_dtype a_dtype);
+
+frt_status frt_gemm_fp8(const uint8_t* a_q, int64_t lda, const float* a_scale,
+                        const void* w_packed, const float* w_scale, const float* bias,
+                        int64_t M, int64_t N, int64_t K, frt_act act, int64_t act_cols,
+                        void* out, int64_t ldo, void* workspace, size_t workspace_bytes,
+                        int* dev_status, frt_stream_t stream);
+
+frt_status frt_gemm_bf16(const void* a, int64_t lda, const void* w_packed, const float* w_scale,
+                         const float* bias, int64_t M, int64_t N, int64_t K, frt_act act,
+                         int64_t act_cols, void* out, int64_t ldo, void* workspace,
+                         size_t workspace_bytes, int* dev_status, frt_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FRT_H_ */

@@ -165,8 +165,8 @@ def encode(x, fmt):
     ((e + bias) << 3) | (n - 8), with n = 16 carrying into the next binade.
     """
     p = _PARAMS[fmt]
-    x = np.asarray(x, dtype=np.float32).astype(np.float64)
-    out = np.zeros(x.shape, dtype=np.int64)
+    with np.errstate(invalid="ignore", over="ignore"):
+        x = np.asarray(x, dtype=np.float32).astype(np.float64)
     nan = np.isnan(x)
     neg = np.signbit(x)
     a = np.abs(np.where(nan, 0.0, x))

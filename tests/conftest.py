@@ -15,14 +15,3 @@ if ROOT not in sys.path:
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a GB300 GPU and the built CUDA library")
-
-
-def within_gemm_tolerance(gpu, ref, sumabs):
-    """The GEMM acceptance bar, per element:
-    |gpu - ref| <= 2^-7 * |ref| + 1e-5 * sum_k |a*w| (scaled)."""
-    import numpy as np
-
-    gpu = np.asarray(gpu, dtype=np.float64)
-    err = np.abs(gpu - ref)
-    bound = 2.0 ** -7 * np.abs(ref) + 1e-5 * sumabs
-    return err <= bound, err, bound
