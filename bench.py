@@ -1,0 +1,636 @@
+#!/usr/bin/env python
+"""Benchmark of the quantized linear-layer path on GB300; prints one JSON line.
+
+Headline step (value, unit TFLOP/s): the encoder-shaped FP8 layer set at
+M = 768 -- (K, N) = (2048, 2560), (2048, 16384), (16384, 2048) -- each layer
+a per-tensor dynamic E4M3 quantize of its bf16 activations (amax + encode)
+followed by the FP8 tcgen05 GEMM with per-channel weight scales and bias,
+all three replayed as one CUDA graph.  value = FP8 GEMM FLOPs of the step x
+steps / device time of the timed region.  R rotating sets of weights,
+activations and outputs (together larger than 4x L2) are cycled so no step
+finds its operands in L2.
+
+Also measured in the same run (``components``): the decoder-shaped GEMMs at
+M = 50, FP8 and BF16, as weight-stream GB/s per layer (weight bytes / kernel
+time, rotating weight copies > 4x L2); the encoder BF16 GEMMs; quantize GB/s
+on 256 Mi Student-t bf16 values; FNUZ -> OCP GB/s on a 1 GiB byte stream;
+and the 18+18-layer synthetic stack's replay latency.
+
+--impl reference times the CPU oracle on the host cores instead (the
+reference arm of the comparison), on bounded samples of the same workload.
+
+Multi-GPU: replicas only (the path has no exchange step); under torchrun
+every rank runs the same step on its own GPU, and value = work of all ranks /
+the slowest rank's time.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = "FP8 GEMM TFLOP/s (M=768) & weight-stream GB/s (M=50) vs roofline; quantize GB/s"
+M_ENC = 768
+M_DEC = 50
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+FP8_OVER_BF16 = 2.0  # nominal dense ratio, 4.5 / 2.25 PFLOP/s
+ENC_WORKLOAD = ("encoder-shaped FP8 layers, M=768, (K,N)=(2048,2560),(2048,16384),(16384,2048): "
+                "per-tensor dynamic OCP E4M3 activation quantize + FP8 GEMM with per-channel "
+                "weight scales and bias, one CUDA graph per step")
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    p.add_argument("--no-components", action="store_true",
+                   help="time the headline step only")
+    p.add_argument("--sweep", action="store_true", help="also run the M sweep at K=N=4096")
+    p.add_argument("--rotate", type=int, default=0,
+                   help="rotating buffer sets for the headline step (0: enough for 4x L2)")
+    return p.parse_args(argv)
+
+
+# ---------------------------------------------------------------- multi-rank plumbing
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")),
+            int(os.environ.get("WORLD_SIZE", "1")))
+
+
+def init_dist(world):
+    if world > 1 and not torch.distributed.is_initialized():
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        torch.distributed.init_process_group(backend)
+
+
+def barrier(world):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def reduce_max(x, world, device=None):
+    """Max of a float over ranks (the slowest rank's time)."""
+    if world == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def reduce_sum(x, world, device=None):
+    if world == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.SUM)
+    return float(t.item())
+
+
+def aggregate(units_per_rank, seconds_per_rank, world, device=None):
+    """Whole-job throughput: units of all ranks / the slowest rank's time."""
+    units = reduce_sum(units_per_rank, world, device)
+    secs = reduce_max(seconds_per_rank, world, device)
+    return units / secs, secs
+
+
+# ---------------------------------------------------------------- peaks and clocks
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples (every 100 ms) while the benchmark runs; the
+    summary keeps the samples taken inside timed regions."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.windows = []
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def window(self, t0, t1):
+        self.windows.append((t0, t1))
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                    ts += float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
+                    rows.append((ts, float(parts[1]), float(parts[2]), parts[5:9]))
+                except (ValueError, IndexError):
+                    continue
+        os.unlink(self.path)
+        inside = [r for r in rows if any(a - 0.15 <= r[0] <= b + 0.15 for a, b in self.windows)]
+        use = inside if inside else rows
+        if not use:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in use for i, v in enumerate(r[3]) if v == "Active"})
+        return {"sm_mhz": statistics.median(r[1] for r in use),
+                "sm_max_mhz": max(r[2] for r in use), "reasons": reasons,
+                "samples": len(use), "in_timed_regions": bool(inside)}
+
+
+# ---------------------------------------------------------------- timing helpers
+
+def device_time(fn, reps, stream=None):
+    """Seconds of device time of reps calls of fn (CUDA events on the
+    launching stream, synchronised on both sides)."""
+    s = stream or torch.cuda.current_stream()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(s)
+    for i in range(reps):
+        fn(i)
+    e1.record(s)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / 1e3
+
+
+def capture(fn):
+    """CUDA graph of fn() (after one eager warm-up on a side stream)."""
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        fn()
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    return g
+
+
+def l2_bytes():
+    return int(getattr(torch.cuda.get_device_properties(torch.cuda.current_device()),
+                       "L2_cache_size", 128 << 20))
+
+
+def bf16_to_dev(bits, device):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(device)
+
+
+# ---------------------------------------------------------------- headline step
+
+class EncoderFP8Set:
+    """One set of encoder-layer weights, inputs and outputs (static buffers)."""
+
+    def __init__(self, src, device):
+        from bf16_gemm_vla_gb300 import layers
+
+        self.layers = []
+        self.inputs = []
+        for lay in src:
+            if isinstance(lay, dict):
+                w = torch.from_numpy(lay["w_f32"]).to(device)
+                b = torch.from_numpy(lay["bias"]).to(device)
+                pw = layers.prepare_fp8(w, b)
+                x = bf16_to_dev(lay["a_bf16"], device)
+            else:  # (Linear, input) of another set: copy to fresh buffers
+                lin0, x0 = lay
+                p = lin0.w
+                pw = layers.PackedWeight(p.packed.clone(), p.K, p.N, p.kind, p.w_scale.clone(),
+                                         p.bias.clone())
+                x = x0.clone()
+            self.layers.append(layers.Linear(pw, M_ENC, act_cols=0, device=device))
+            self.inputs.append(x)
+
+    def forward(self):
+        for lin, x in zip(self.layers, self.inputs):
+            lin(x)
+
+    def flops(self):
+        return sum(2.0 * M_ENC * lin.w.K * lin.w.N for lin in self.layers)
+
+    def nbytes(self):
+        n = 0
+        for lin, x in zip(self.layers, self.inputs):
+            n += lin.w.packed.numel() + x.numel() * 2 + lin.out.numel() * 2 + lin.q.numel()
+        return n
+
+
+def kernel_durations(sets, iters):
+    """Per-layer device durations of the quantize (amax + encode) and of the
+    GEMM, from events around each launch; the GPU is held busy first so the
+    whole sequence is queued before it runs back to back."""
+    from bf16_gemm_vla_gb300 import frt
+
+    nl = len(sets[0].layers)
+    ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(nl)]
+          for _ in range(iters)]
+    torch.cuda.synchronize()
+    torch.cuda._sleep(400_000_000)  # ~0.2 s at 2 GHz: longer than the enqueue below
+    for it in range(iters):
+        st = sets[it % len(sets)]
+        for li, (lin, x) in enumerate(zip(st.layers, st.inputs)):
+            ev[it][li][0].record()
+            frt.frt_quantize_e4m3(x, frt.PER_TENSOR, frt.OCP, q=lin.q, scale=lin.a_scale,
+                                  workspace=lin.ws)
+            ev[it][li][1].record()
+            frt.frt_gemm_fp8(lin.q, lin.a_scale, lin.w.packed, lin.w.w_scale, lin.w.N,
+                             bias=lin.w.bias, out=lin.out)
+            ev[it][li][2].record()
+    torch.cuda.synchronize()
+    quant = [[ev[it][li][0].elapsed_time(ev[it][li][1]) / 1e3 for it in range(iters)]
+             for li in range(nl)]
+    gemm = [[ev[it][li][1].elapsed_time(ev[it][li][2]) / 1e3 for it in range(iters)]
+            for li in range(nl)]
+    return quant, gemm
+
+
+def run_headline(args, device, world, sampler, peaks, peak_kind):
+    from bf16_gemm_vla_gb300 import frt
+
+    src = synth.encoder(seed=0, M=M_ENC)
+    set0 = EncoderFP8Set(src, device)
+    per_set = set0.nbytes()
+    R = args.rotate or max(2, -(-4 * l2_bytes() // per_set))
+    sets = [set0] + [EncoderFP8Set(list(zip(set0.layers, set0.inputs)), device)
+                     for _ in range(R - 1)]
+    torch.cuda.synchronize()  # weight copies complete before the GEMMs read them
+    graphs = [capture(s.forward) for s in sets]
+    flops = set0.flops()
+    for i in range(args.warmup):
+        graphs[i % R].replay()
+    barrier(world)
+    t0 = time.time()
+    secs = device_time(lambda i: graphs[i % R].replay(), args.steps)
+    sampler.window(t0, time.time())
+    barrier(world)
+    frt.check_device_status()
+    value, secs_max = aggregate(flops * args.steps, secs, world, device)
+
+    # per-kernel durations for the roofline
+    iters = min(100, max(10, args.steps // 10))
+    t0 = time.time()
+    quant, gemm = kernel_durations(sets, iters)
+    sampler.window(t0, time.time())
+    layers_out = []
+    tot_flops = 0.0
+    tot_time = 0.0
+    for li, lin in enumerate(set0.layers):
+        g = statistics.mean(gemm[li])
+        q = statistics.mean(quant[li])
+        f = 2.0 * M_ENC * lin.w.K * lin.w.N
+        tot_flops += f
+        tot_time += g
+        layers_out.append({"K": lin.w.K, "N": lin.w.N, "gemm_us": g * 1e6,
+                           "gemm_tflops": f / g / 1e12, "quantize_us": q * 1e6})
+    fp8_peak = peaks["bf16_tflops_sustained"] * FP8_OVER_BF16
+    achieved = tot_flops / tot_time / 1e12
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": fp8_peak, "unit": "TFLOP/s",
+                "frac": achieved / fp8_peak, "traffic": None,
+                "kernel": "gemm_tc_kernel<fp8, 128x256 tiles>",
+                "peak_source": "%s bf16 sustained x %.0f (nominal FP8/BF16 dense ratio), of %s"
+                               % (peak_kind, FP8_OVER_BF16, peak_kind),
+                "per_launch_flops": tot_flops / len(set0.layers)}
+
+    # end to end through the public API: pinned host inputs -> device, graph
+    # replay, outputs -> pinned host, every step
+    h_in = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in set0.inputs]
+    for h, x in zip(h_in, set0.inputs):
+        h.copy_(x)
+    h_out = [torch.empty(l.out.shape, dtype=l.out.dtype, pin_memory=True) for l in set0.layers]
+    h2d = sum(h.numel() * h.element_size() for h in h_in)
+    d2h = sum(h.numel() * h.element_size() for h in h_out)
+
+    def e2e_step(i):
+        st = sets[i % R]
+        for h, x in zip(h_in, st.inputs):
+            x.copy_(h, non_blocking=True)
+        graphs[i % R].replay()
+        for h, lin in zip(h_out, st.layers):
+            h.copy_(lin.out, non_blocking=True)
+
+    e2e_steps = max(10, min(args.steps, 500))
+    for i in range(min(args.warmup, 5)):
+        e2e_step(i)
+    barrier(world)
+    t0 = time.time()
+    e2e_secs = device_time(e2e_step, e2e_steps)
+    sampler.window(t0, time.time())
+    e2e_value, _ = aggregate(flops * e2e_steps, e2e_secs, world, device)
+
+    cfg = {"workload": ENC_WORKLOAD, "M": M_ENC,
+           "layers": [[lin.w.K, lin.w.N] for lin in set0.layers],
+           "weights": "N(0,0.02) fp32 -> per-channel OCP E4M3; A ~ N(0,1) bf16 with 1% x50 "
+                      "outliers; bias N(0,0.1); seed 0",
+           "l2": "inputs larger than L2: %d rotating sets of weights+activations+outputs, "
+                 "%.0f MB in total (L2 %.0f MB)" % (R, R * per_set / 1e6, l2_bytes() / 1e6),
+           "parallelism": "replicas" if world > 1 else "single GPU"}
+    return {
+        "value": value / 1e12, "secs": secs_max, "flops_per_step": flops, "config": cfg,
+        "roofline": roofline, "layers": layers_out,
+        "e2e": {"value": e2e_value / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "launches_per_step": 3 * len(set0.layers),
+    }
+
+
+# ---------------------------------------------------------------- components
+
+def gemm_stream_rate(lay, kind, device, sampler, reps=3):
+    """Per-launch device time of one layer's GEMM, over rotating weight copies
+    (total > 4x L2) captured back to back in one graph."""
+    from bf16_gemm_vla_gb300 import frt, layers
+
+    w = torch.from_numpy(lay["w_f32"]).to(device)
+    b = torch.from_numpy(lay["bias"]).to(device)
+    x = bf16_to_dev(lay["a_bf16"], device)
+    pw = layers.prepare_fp8(w, b) if kind == "e4m3" else layers.prepare_bf16(w, b)
+    wbytes = pw.packed.numel()
+    copies = max(4, -(-4 * l2_bytes() // wbytes))
+    copies = min(copies, 256)
+    packs = [pw.packed] + [pw.packed.clone() for _ in range(copies - 1)]
+    torch.cuda.synchronize()  # weight copies complete before the GEMMs read them
+    lin = layers.Linear(pw, lay["M"], act_cols=lay["act_cols"], device=device)
+    if kind == "e4m3":
+        frt.frt_quantize_e4m3(x, frt.PER_TENSOR, frt.OCP, q=lin.q, scale=lin.a_scale,
+                              workspace=lin.ws)
+
+    def run_all():
+        for p in packs:
+            if kind == "e4m3":
+                frt.frt_gemm_fp8(lin.q, lin.a_scale, p, pw.w_scale, pw.N, bias=b,
+                                 act_cols=lay["act_cols"], out=lin.out)
+            else:
+                frt.frt_gemm_bf16(x, p, pw.N, bias=b, act_cols=lay["act_cols"], out=lin.out)
+
+    g = capture(run_all)
+    g.replay()
+    t0 = time.time()
+    secs = device_time(lambda i: g.replay(), reps)
+    sampler.window(t0, time.time())
+    per = secs / (reps * copies)
+    flops = 2.0 * lay["M"] * lay["K"] * lay["N"]
+    del packs, g
+    return {"K": lay["K"], "N": lay["N"], "us": per * 1e6, "weight_bytes": wbytes,
+            "weight_gbs": wbytes / per / 1e9, "tflops": flops / per / 1e12, "copies": copies}
+
+
+def run_components(args, device, sampler, peaks):
+    from bf16_gemm_vla_gb300 import frt
+    from bf16_gemm_vla_gb300.stack import SyntheticStack
+
+    out = {}
+    hbm = peaks["hbm_gbs"]
+    # decoder-shaped GEMMs, weight-stream GB/s
+    dec = synth.decoder(seed=0, M=M_DEC)
+    for kind in ("e4m3", "bf16"):
+        rows = [gemm_stream_rate(lay, kind, device, sampler) for lay in dec]
+        tb = sum(r["weight_bytes"] for r in rows)
+        tt = sum(r["us"] for r in rows) / 1e6
+        out["decoder_m50_" + ("fp8" if kind == "e4m3" else "bf16")] = {
+            "layers": rows, "weight_gbs": tb / tt / 1e9, "frac_of_hbm": tb / tt / 1e9 / hbm}
+    # encoder-shaped BF16 GEMMs
+    enc = synth.encoder(seed=0, M=M_ENC)
+    rows = [gemm_stream_rate(lay, "bf16", device, sampler, reps=2) for lay in enc]
+    tf = sum(2.0 * M_ENC * r["K"] * r["N"] for r in rows)
+    tt = sum(r["us"] for r in rows) / 1e6
+    out["encoder_m768_bf16"] = {"layers": rows, "tflops": tf / tt / 1e12,
+                                "frac_of_bf16_peak": tf / tt / 1e12 / peaks["bf16_tflops_sustained"]}
+    del enc
+    # quantize, 256 Mi Student-t bf16 (two passes: 2 B + 2 B read, 1 B written)
+    n = 256 << 20
+    x = bf16_to_dev(synth.student_t_bf16(n, seed=3).reshape(-1, 4096), device)
+    q = torch.empty(x.shape, dtype=torch.uint8, device=device)
+    s = torch.empty(1, dtype=torch.float32, device=device)
+    ws = torch.empty(frt.frt_quantize_workspace_bytes(x.shape[0], x.shape[1]) // 4,
+                     dtype=torch.float32, device=device)
+
+    def quant(i):
+        frt.frt_quantize_e4m3(x, frt.PER_TENSOR, frt.OCP, q=q, scale=s, workspace=ws)
+
+    quant(0)
+    t0 = time.time()
+    secs = device_time(quant, 10) / 10
+    sampler.window(t0, time.time())
+    out["quantize_256Mi_bf16"] = {"us": secs * 1e6, "gbs_5B_per_elem": 5.0 * n / secs / 1e9,
+                                  "gbs_3B_per_elem": 3.0 * n / secs / 1e9,
+                                  "frac_of_hbm": 5.0 * n / secs / 1e9 / hbm}
+    del x, q
+    # FNUZ -> OCP over 1 GiB
+    nb = 1 << 30
+    src = torch.from_numpy(synth.uniform_bytes(nb, seed=2)).to(device)
+    dst = torch.empty_like(src)
+    frt.frt_fnuz_to_ocp(src, out=dst)
+    t0 = time.time()
+    secs = device_time(lambda i: frt.frt_fnuz_to_ocp(src, out=dst), 10) / 10
+    sampler.window(t0, time.time())
+    out["fnuz_to_ocp_1GiB"] = {"us": secs * 1e6, "gbs": 2.0 * nb / secs / 1e9,
+                               "frac_of_hbm": 2.0 * nb / secs / 1e9 / hbm}
+    del src, dst
+    torch.cuda.empty_cache()
+    # the synthetic 18+18-layer stack, one CUDA graph per replay
+    st = SyntheticStack(n_layers=18, seed=1, device=device, keep=())
+    xe, xd = synth.stack_inputs(seed=1)
+    st.x_enc.copy_(bf16_to_dev(xe, device))
+    st.x_dec.copy_(bf16_to_dev(xd, device))
+    st.capture()
+    st.replay()
+    t0 = time.time()
+    secs = device_time(lambda i: st.replay(), 10) / 10
+    sampler.window(t0, time.time())
+    frt.check_device_status()
+    out["stack_18enc_fp8_18dec_bf16"] = {"ms_per_replay": secs * 1e3,
+                                         "launches_per_replay": st.launches_per_forward(),
+                                         "weight_bytes": st.weight_bytes()}
+    del st
+    torch.cuda.empty_cache()
+    if args.sweep:
+        sw = []
+        for M in synth.SWEEP_M:
+            lay = synth.sweep_gemm(M, seed=M)
+            a = gemm_stream_rate(lay, "e4m3", device, sampler, reps=2)
+            b = gemm_stream_rate(lay, "bf16", device, sampler, reps=2)
+            sw.append({"M": M, "fp8_us": a["us"], "bf16_us": b["us"], "fp8_tflops": a["tflops"],
+                       "bf16_tflops": b["tflops"], "fp8_weight_gbs": a["weight_gbs"],
+                       "bf16_weight_gbs": b["weight_gbs"]})
+        out["sweep_k4096_n4096"] = sw
+    return out
+
+
+# ---------------------------------------------------------------- CPU oracle (baseline / reference arm)
+
+def oracle_sample_step(src, rows, cols):
+    """One sample of the headline step on the CPU oracle: per encoder layer,
+    quantize `rows` activation rows, then the FP8 layer on the first `cols`
+    output channels (weights quantized at load).  Returns FLOPs done."""
+    from oracle import e4m3, gemm, quantize
+
+    flops = 0.0
+    for lay in src:
+        a = synth.bf16_bits_as_f32(lay["a_bf16"][:rows])
+        qa, sa = quantize.quantize_e4m3(a, quantize.PER_TENSOR, e4m3.OCP)
+        qw, sw = lay["_oracle_w"]
+        gemm.gemm_fp8(qa, e4m3.OCP, sa, qw[:, :cols], e4m3.OCP, sw[:cols], lay["bias"][:cols], 0)
+        flops += 2.0 * rows * lay["K"] * cols
+    return flops
+
+
+def oracle_setup(cols):
+    from oracle import e4m3, quantize
+
+    src = synth.encoder(seed=0, M=M_ENC)
+    for lay in src:
+        lay["_oracle_w"] = quantize.quantize_e4m3(lay["w_f32"][:, :cols], quantize.PER_COL,
+                                                  e4m3.OCP)
+    return src
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+def cpu_baseline(budget_s=12.0, rows=16, cols=256):
+    src = oracle_setup(cols)
+    oracle_sample_step(src, rows, cols)  # warm
+    flops = 0.0
+    t0 = time.perf_counter()
+    n = 0
+    while time.perf_counter() - t0 < budget_s:
+        flops += oracle_sample_step(src, rows, cols)
+        n += 1
+    secs = time.perf_counter() - t0
+    return {"value": flops / secs / 1e12, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
+            "sample": "%d steps of %d activation rows x the first %d output channels of each "
+                      "encoder layer (quantize + fp64 GEMM + epilogue), %.1f s" % (n, rows, cols, secs)}
+
+
+def run_reference(args):
+    rank, _, world = dist_env()
+    if rank != 0:
+        return 0
+    rows = 16
+    cols = 256
+    src = oracle_setup(cols)
+    t0 = time.perf_counter()
+    oracle_sample_step(src, rows, cols)
+    one = time.perf_counter() - t0
+    budget = 150.0 / max(1, args.steps + args.warmup)
+    while one > budget and cols > 16:
+        cols //= 2
+        one /= 2
+    src = oracle_setup(cols)
+    for _ in range(args.warmup):
+        oracle_sample_step(src, rows, cols)
+    t0 = time.perf_counter()
+    flops = 0.0
+    for _ in range(args.steps):
+        flops += oracle_sample_step(src, rows, cols)
+    secs = time.perf_counter() - t0
+    value = flops / secs / 1e12
+    sample = ("%d activation rows x the first %d output channels of each encoder layer per step "
+              "(quantize + fp64 GEMM + epilogue)" % (rows, cols))
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": secs / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": ENC_WORKLOAD + " (CPU oracle, bounded sample)", "M": M_ENC,
+                       "sample": sample},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cpu_cores(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+# ---------------------------------------------------------------- main
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    rank, local_rank, world = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device (GB300); the library has no CPU path")
+    torch.cuda.set_device(local_rank)
+    device = torch.device("cuda", local_rank)
+    init_dist(world)
+    from bf16_gemm_vla_gb300 import build
+
+    if rank == 0:
+        build.build()
+    barrier(world)
+    peaks, peak_kind = load_peaks()
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    try:
+        head = run_headline(args, device, world, sampler, peaks, peak_kind)
+        comps = None if args.no_components else run_components(args, device, sampler, peaks)
+    finally:
+        clocks = sampler.stop()
+    cpu = cpu_baseline() if (rank == 0 and world == 1) else None
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": head["value"], "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": head["secs"] / args.steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "e4m3", "data": "synthetic",
+            "config": head["config"], "roofline": head["roofline"], "cpu_baseline": cpu,
+            "e2e": head["e2e"], "gpu_launches": head["launches_per_step"] * args.steps,
+            "clocks": clocks, "layers": head["layers"], "components": comps,
+            "peaks": {"source": peak_kind, "hbm_gbs": peaks["hbm_gbs"],
+                      "bf16_tflops": peaks["bf16_tflops"],
+                      "bf16_tflops_sustained": peaks["bf16_tflops_sustained"],
+                      "fp8_tflops_sustained": peaks["bf16_tflops_sustained"] * FP8_OVER_BF16},
+        }
+        print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

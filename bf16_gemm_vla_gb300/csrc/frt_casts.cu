@@ -7,6 +7,7 @@
 // DeepSeek-V4-Flash on AMD MI300X", "The FP8 dialect problem").
 #include <cuda_bf16.h>
 
+#include "frt_device.cuh"
 #include "frt_host.h"
 
 namespace frt {
@@ -189,6 +190,8 @@ __global__ void __launch_bounds__(kQThreads) encode_tensor_kernel(
     uint8_t* __restrict__ q, float* __restrict__ scale_out) {
   __shared__ float red[32];
   __shared__ float s_sh;
+  // a GEMM launched after this grid may start fetching its weights now
+  dev::grid_launch_dependents();
   if (static_scale) {
     if (threadIdx.x == 0) s_sh = __ldg(static_scale);
   } else {
@@ -250,6 +253,7 @@ __global__ void __launch_bounds__(kQThreads) encode_col_kernel(
     const T* __restrict__ x, int64_t rows, int64_t cols, int64_t ldx,
     const float* __restrict__ partial, int npartial, const float* __restrict__ static_scale,
     uint8_t* __restrict__ q, float* __restrict__ scale_out) {
+  dev::grid_launch_dependents();
   const int64_t c = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (c >= cols) return;
   float s;

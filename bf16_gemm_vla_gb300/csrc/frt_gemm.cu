@@ -14,21 +14,31 @@
 //   * small M ("swap" tiles): the product is taken transposed,
 //     out^T = W^T . A^T, so the MMA's 128 rows cover output channels and
 //     the few activation rows become the MMA N dimension (32/64/128).  The
-//     weight tile is the operand that streams; every CTA reads 16 KiB
-//     contiguous per pipeline stage.
+//     weight tile is the operand that streams; every pipeline stage reads a
+//     16 KiB contiguous packed tile.
 //
 // Both operands are K-major with the 128-byte swizzle.  Activations arrive
-// by TMA (tensor map, zero fill past M and K); weights are pre-packed into
-// the exact shared-memory image (see frt_pack.cu) and arrive by plain bulk
-// copies.  Warp roles: warp 0 issues the copies, one thread of warp 1
-// issues tcgen05.mma into a TMEM accumulator, warps 2-5 run the epilogue.
+// by TMA (zero fill past M and K); weights are pre-packed into the exact
+// shared-memory image (frt_pack.cu) and arrive by plain bulk copies.  Warp
+// roles: warp 0 issues the copies, one thread of warp 1 issues tcgen05.mma
+// into TMEM, warps 2-5 run the epilogue, which stages bf16 results in
+// swizzled shared memory and writes them with TMA tensor stores.
 //
-// When there are fewer output tiles than SMs, K is split across the CTAs of
-// a thread-block cluster (grid z = cluster z = splits).  Each CTA writes its
-// fp32 partial tile to its own shared memory; after a cluster barrier every
-// CTA reduces a slice of the tile over all ranks, in rank order (so the
-// result does not depend on timing), and applies the epilogue.  No global
-// workspace and no atomics are involved.
+// Scheduling:
+//   * without split-K the grid is persistent (one CTA per SM walks a
+//     strided tile list) and the TMEM accumulator is double-buffered, so a
+//     tile's epilogue overlaps the next tile's mainloop;
+//   * when there are fewer output tiles than SMs, K is split across the
+//     CTAs of a thread-block cluster.  The tile's columns are cut into
+//     chunks, each owned by one CTA; every CTA pushes the chunks it does not
+//     own, straight from registers, into the owner's shared memory
+//     (st.async, counted on the owner's mbarrier), and the owner adds the
+//     partial sums in rank order -- a fixed order, so the result does not
+//     depend on timing -- and stores the chunk.
+//
+// With programmatic dependent launch, the first pipeline stages' weight
+// tiles (static data) are fetched before the kernel waits for the previous
+// grid; activations and the activation scale are read only after the wait.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -41,27 +51,35 @@
 namespace frt {
 namespace {
 
-constexpr int kThreads = 192;       // 6 warps: copy, MMA, 4 x epilogue
-constexpr int kTile = 128;          // MMA M; channels per packed weight tile
-constexpr int kKBytes = 128;        // bytes of K per pipeline stage
+constexpr int kThreads = 192;            // 6 warps: copy, MMA, 4 x epilogue
+constexpr int kTile = 128;               // MMA M; channels per packed weight tile
+constexpr int kKBytes = 128;             // bytes of K per pipeline stage
 constexpr int kWTile = kTile * kKBytes;  // bytes of one packed weight tile
-constexpr int kPipeBudget = 196608;      // shared memory for the stages
-constexpr int kPitch = 129;         // floats per column of a split-K partial tile
-constexpr int kMaxSplits = 8;       // portable cluster size
+constexpr int kSmemMax = 232448;         // dynamic shared memory limit per CTA
+constexpr int kWarpOutBytes = 2048;      // one warp's bf16 output staging buffer
+constexpr int kOutBytes = 4 * 2 * kWarpOutBytes;  // 4 epilogue warps x 2 buffers
+constexpr int kBarRegion = 512;          // mbarriers, TMEM address, abort flag
+constexpr int kMaxSplits = 8;            // portable cluster size
+constexpr int kMaxStages = 8;
 
 struct GemmArgs {
   const uint8_t* w_packed;
   const float* a_scale;  // 1 float or null (= 1)
   const float* w_scale;  // N floats or null (= 1)
   const float* bias;     // N floats or null (= 0)
-  __nv_bfloat16* out;
-  int64_t ldo;
   int M, N;
   int act_cols;
   int kb_total;  // 128-byte K blocks of the packed weight
   int nb_total;  // 128-channel groups of the packed weight
   int kb_per_split;
   int splits;
+  int tiles_m, tiles_n, num_tiles;
+  int stages;          // pipeline depth
+  int chunk_cols;      // split-K: TMEM columns per chunk (32 large M, 8 small M)
+  int recv_in_stages;  // split-K: receive buffers reuse the stage buffers
+  int outbuf_off;      // shared-memory layout (bytes from the 1024-aligned base)
+  int recv_off;
+  int tail_off;        // per-channel scale/bias, then mbarriers
   int* dev_status;
 };
 
@@ -72,15 +90,10 @@ struct Cfg {
   static constexpr int kActBytes = kActRows * kKBytes;
   static constexpr int kWBytes = kWRows * kKBytes;
   static constexpr int kStageBytes = kActBytes + kWBytes;
-  static constexpr int kStages = (kPipeBudget / kStageBytes) > 8 ? 8 : (kPipeBudget / kStageBytes);
-  static constexpr int kPipeBytes = kStages * kStageBytes;
-  static constexpr int kTmemCols = kBN;
-  static constexpr int kPartialBytes = kBN * kPitch * 4;
-  static constexpr int kSmemBytes = 1024 + kPipeBytes + 256;
+  static constexpr int kTmemCols = kSwap ? 2 * kBN : 512;  // two accumulator buffers
   static_assert(kActBytes % 1024 == 0 && kWBytes % 1024 == 0, "operand tiles 1024-aligned");
-  static_assert(kPartialBytes <= kPipeBytes, "partial tile fits in the stage buffers");
-  static_assert(kBN == 32 || kBN == 64 || kBN == 128 || kBN == 256, "TMEM columns");
-  static_assert(kStages >= 2, "pipeline depth");
+  static_assert(kBN == 32 || kBN == 64 || kBN == 128 || kBN == 256, "tile width");
+  static_assert(kSwap || kBN == 256, "large-M tiles are 128 x 256");
 };
 
 __device__ __forceinline__ float gelu_tanh(float v) {
@@ -94,229 +107,454 @@ __device__ __forceinline__ float epi(float acc, float cs, float b, bool act) {
   return act ? gelu_tanh(v) : v;
 }
 
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// Stages one warp's part of a bf16 output chunk in shared memory and
+// writes it with a TMA tensor store (64-byte swizzle, 64-byte rows).
+//   large M: 32 rows (the warp's TMEM lanes) x 32 channels; lane = row,
+//     v[j] = channel x0 + j; box {32 ch, 32 rows}.
+//   small M: kRows activation rows x 32 channels (the warp's lanes); lane =
+//     channel x0 + lane, v[j] = row y0 + j; box {32 ch, kRows}.
+// Each warp owns two staging buffers and alternates between them; lane 0
+// issues the store and keeps the buffer's previous store tracked.
+template <bool kSwap, int kRows>
+__device__ __forceinline__ void warp_store(const float* v, uint8_t* buf, uint32_t buf_s,
+                                           const CUtensorMap* tmap, int x0, int y0, int lane) {
+  if (lane == 0) dev::bulk_wait_read<1>();  // this buffer's previous store has read it
+  __syncwarp();
+  if constexpr (!kSwap) {
+    uint8_t* rowp = buf + lane * 64;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      uint4 w;
+      w.x = pack_bf16x2(v[8 * q + 0], v[8 * q + 1]);
+      w.y = pack_bf16x2(v[8 * q + 2], v[8 * q + 3]);
+      w.z = pack_bf16x2(v[8 * q + 4], v[8 * q + 5]);
+      w.w = pack_bf16x2(v[8 * q + 6], v[8 * q + 7]);
+      *reinterpret_cast<uint4*>(rowp + ((q ^ ((lane >> 1) & 3)) << 4)) = w;
+    }
+  } else {
+    const int cb = lane * 2;  // byte of this channel in a 64-byte row
+#pragma unroll
+    for (int j = 0; j < kRows; ++j)
+      *reinterpret_cast<__nv_bfloat16*>(buf + j * 64 + (((cb >> 4) ^ ((j >> 1) & 3)) << 4) +
+                                        (cb & 15)) = __float2bfloat16_rn(v[j]);
+  }
+  dev::fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    dev::tma_store_2d(tmap, buf_s, x0, y0);
+    dev::bulk_commit();
+  }
+}
+
+// Byte offset of float4 granule q of row r in a split-K partial chunk of
+// 128 rows x cw floats (cw = 32 or 8); granules are XOR-swizzled by row so
+// that row-per-thread reads and writes are free of bank conflicts.
+__device__ __forceinline__ uint32_t chunk_off(int r, int q, int cw) {
+  const int swz = cw == 32 ? (r & 7) : ((r >> 2) & 1);
+  return static_cast<uint32_t>(r * cw * 4 + ((q ^ swz) << 4));
+}
+
 template <bool kFp8, bool kSwap, int kBN>
 __global__ void __launch_bounds__(kThreads, 1)
-    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_act, const GemmArgs p) {
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_act,
+                   const __grid_constant__ CUtensorMap tmap_out, const GemmArgs p) {
   using C = Cfg<kSwap, kBN>;
-  constexpr int kStages = C::kStages;
   constexpr int kEsize = kFp8 ? 1 : 2;
+  const int stages = p.stages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const uint32_t sbase = dev::smem_u32(base);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(base + C::kPipeBytes);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 1);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float* col_sb = reinterpret_cast<float*>(base + p.tail_off);  // [2 bufs][scale, bias][kBN]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(col_sb + 4 * kBN);
   const uint32_t full0 = dev::smem_u32(bars);
-  const uint32_t empty0 = full0 + 8 * kStages;
-  const uint32_t accum_bar = full0 + 16 * kStages;
+  const uint32_t empty0 = full0 + 8 * stages;
+  const uint32_t tfull0 = empty0 + 8 * stages;
+  const uint32_t tempty0 = tfull0 + 16;
+  const uint32_t recv_bar = tempty0 + 16;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * stages + 5);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const bool split = p.splits > 1;
+  const int S = p.splits;
+  const int rank = split ? static_cast<int>(dev::cluster_ctarank()) : 0;
+
+  // split-K chunks: chunk_cols TMEM columns each; rank j owns chunks
+  // [cb(j), cb(j+1)) with cb(j) = ceil(j * NC / S)
+  const int CW = p.chunk_cols;
+  const int NC = split ? kBN / CW : 1;
+  auto chunk_begin = [&](int j) { return (j * NC + S - 1) / S; };
+  const int owned_max = split ? (NC + S - 1) / S : 0;
+  const uint32_t chunk_bytes = static_cast<uint32_t>(kTile * CW * 4);
+  const int own_c0 = split ? chunk_begin(rank) : 0;
+  const int own_c1 = split ? chunk_begin(rank + 1) : 0;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < stages; ++s) {
       dev::mbar_init(full0 + 8 * s, 1);
       dev::mbar_init(empty0 + 8 * s, 1);
     }
-    dev::mbar_init(accum_bar, 1);
+    dev::mbar_init(tfull0, 1);
+    dev::mbar_init(tfull0 + 8, 1);
+    dev::mbar_init(tempty0, 4);
+    dev::mbar_init(tempty0 + 8, 4);
+    dev::mbar_init(recv_bar, 1);
     *abort_flag = 0;
     dev::fence_mbar_init();
+    if (split)  // bytes this CTA receives: its own chunks from every peer
+      dev::mbar_arrive_expect_tx(recv_bar, static_cast<uint32_t>(S - 1) *
+                                               static_cast<uint32_t>(own_c1 - own_c0) *
+                                               chunk_bytes);
     dev::prefetch_tmap(&tmap_act);
+    dev::prefetch_tmap(&tmap_out);
   }
   if (warp == 1) dev::tmem_alloc(dev::smem_u32(tmem_slot), C::kTmemCols);
   dev::tc_fence_before();
   __syncthreads();
   dev::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // the next grid on the stream may start its prologue (it waits for this
+  // grid's completion before it reads or writes anything this grid touches)
+  dev::grid_launch_dependents();
+  // Split-K cluster barrier, phase 1: with dedicated receive buffers every
+  // thread arrives now (its mbarriers are initialised); when the receive
+  // buffers reuse the stage buffers, each thread arrives once this CTA's
+  // MMAs can no longer read them.
+  if (split && !p.recv_in_stages) dev::cluster_arrive();
 
-  const int split = blockIdx.z;
-  const int kb0 = split * p.kb_per_split;
-  const int nkb = min(p.kb_per_split, p.kb_total - kb0);
-  const int tile_n = blockIdx.x;
-  const int tile_m = blockIdx.y;
+  // this CTA's tiles: split -> one tile and a K range; else a strided list
+  const int kb0 = split ? rank * p.kb_per_split : 0;
+  const int nkb = split ? min(p.kb_per_split, p.kb_total - kb0) : p.kb_total;
+  const int t_step = split ? p.num_tiles : static_cast<int>(gridDim.x);
+  const int my_tiles =
+      split ? 1 : (p.num_tiles - static_cast<int>(blockIdx.x) + t_step - 1) / t_step;
+  auto tile_of = [&](int it, int& tm, int& tn) {
+    const int t = static_cast<int>(blockIdx.x) + it * t_step;
+    if (kSwap) {
+      tn = t % p.tiles_n;
+      tm = t / p.tiles_n;
+    } else {  // rows fastest: the CTAs that share a weight tile run together
+      tm = t % p.tiles_m;
+      tn = t / p.tiles_m;
+    }
+  };
 
-  if (warp == 0 && lane == 0) {
-    // ---------------------------------------------------------------- copies
-    const uint64_t pol_w = dev::policy_evict_first();
-    const uint64_t pol_a = dev::policy_evict_last();
-    const int act_row0 = tile_m * C::kActRows;
-    const int nb_first = kSwap ? tile_n : tile_n * (kBN / kTile);
-    const int groups = kSwap ? 1 : min(kBN / kTile, p.nb_total - nb_first);
-    const uint32_t tx = C::kActBytes + groups * kWTile;
-    int issued = 0;
-    for (int i = 0; i < nkb; ++i) {
-      const int s = i % kStages;
-      const uint32_t ph = (i / kStages) & 1;
-      if (!dev::mbar_wait(empty0 + 8 * s, ph ^ 1, abort_flag, p.dev_status,
-                          dev::kTimeoutProducer))
-        break;
-      const uint32_t st = sbase + s * C::kStageBytes;
-      dev::mbar_arrive_expect_tx(full0 + 8 * s, tx);
-      const int kb = kb0 + i;
-      dev::tma_load_2d(st, &tmap_act, kb * (kKBytes / kEsize), act_row0, full0 + 8 * s, pol_a);
-      for (int g = 0; g < groups; ++g) {
-        const uint8_t* src =
-            p.w_packed + (static_cast<size_t>(nb_first + g) * p.kb_total + kb) * kWTile;
-        dev::bulk_load(st + C::kActBytes + g * kWTile, src, kWTile, full0 + 8 * s, pol_w);
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ copies
+      const uint64_t pol_w = kSwap ? dev::policy_evict_first() : dev::policy_evict_normal();
+      const uint64_t pol_a = dev::policy_evict_last();
+      const int total = my_tiles * nkb;
+      // geometry of flat k-block g: tile rows, first weight group, groups, tx bytes
+      auto geom = [&](int g, int& tm, int& nbf, int& groups) -> uint32_t {
+        int tn;
+        tile_of(g / nkb, tm, tn);
+        nbf = kSwap ? tn : tn * (kBN / kTile);
+        groups = kSwap ? 1 : min(kBN / kTile, p.nb_total - nbf);
+        return static_cast<uint32_t>(C::kActBytes + groups * kWTile);
+      };
+      auto load_weights = [&](int g, int s, int nbf, int groups) {
+        const uint32_t st = sbase + s * C::kStageBytes;
+        const int kb = kb0 + g % nkb;
+        for (int q = 0; q < groups; ++q) {
+          const uint8_t* src =
+              p.w_packed + (static_cast<size_t>(nbf + q) * p.kb_total + kb) * kWTile;
+          dev::bulk_load(st + C::kActBytes + q * kWTile, src, kWTile, full0 + 8 * s, pol_w);
+        }
+      };
+      auto load_act = [&](int g, int s, int tm) {
+        dev::tma_load_2d(sbase + s * C::kStageBytes, &tmap_act,
+                         (kb0 + g % nkb) * (kKBytes / kEsize), tm * C::kActRows, full0 + 8 * s,
+                         pol_a);
+      };
+      const int npre = total < stages ? total : stages;
+      for (int g = 0; g < npre; ++g) {  // first use of each stage needs no wait
+        int tm, nbf, groups;
+        const uint32_t tx = geom(g, tm, nbf, groups);
+        dev::mbar_arrive_expect_tx(full0 + 8 * g, tx);
+        load_weights(g, g, nbf, groups);
       }
-      issued = i + 1;
+      dev::grid_dependency_wait();
+      for (int g = 0; g < npre; ++g) {
+        int tm, nbf, groups;
+        geom(g, tm, nbf, groups);
+        load_act(g, g, tm);
+      }
+      int issued = npre;
+      int s = npre % stages;
+      uint32_t ph = static_cast<uint32_t>(npre / stages);
+      for (int g = npre; g < total; ++g) {
+        if (!dev::mbar_wait(empty0 + 8 * s, (ph & 1) ^ 1, abort_flag, p.dev_status,
+                            dev::kTimeoutProducer))
+          break;
+        int tm, nbf, groups;
+        const uint32_t tx = geom(g, tm, nbf, groups);
+        dev::mbar_arrive_expect_tx(full0 + 8 * s, tx);
+        load_weights(g, s, nbf, groups);
+        load_act(g, s, tm);
+        issued = g + 1;
+        if (++s == stages) {
+          s = 0;
+          ++ph;
+        }
+      }
+      // Do not leave with copies in flight: wait (bounded, even after an
+      // abort) for the last use of every stage that was armed.
+      for (int g = issued - stages < 0 ? 0 : issued - stages; g < issued; ++g)
+        dev::mbar_wait(full0 + 8 * (g % stages), (g / stages) & 1, nullptr, p.dev_status,
+                       dev::kTimeoutProducer);
     }
-    // Do not leave with copies in flight: wait (bounded, even after an
-    // abort) for the last use of every stage that was armed.
-    for (int i = issued - kStages < 0 ? 0 : issued - kStages; i < issued; ++i) {
-      const int s = i % kStages;
-      const uint32_t ph = (i / kStages) & 1;
-      dev::mbar_wait(full0 + 8 * s, ph, nullptr, p.dev_status, dev::kTimeoutProducer);
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ MMA
+      constexpr uint32_t idesc = dev::instr_desc(kFp8, kTile, kBN);
+      int s = 0;
+      uint32_t ph = 0;
+      for (int it = 0; it < my_tiles; ++it) {
+        const int b = it & 1;
+        const uint32_t u = static_cast<uint32_t>(it >> 1);
+        if (!dev::mbar_wait(tempty0 + 8 * b, (u & 1) ^ 1, abort_flag, p.dev_status,
+                            dev::kTimeoutMma))
+          break;
+        dev::tc_fence_after();
+        const uint32_t d = tmem + static_cast<uint32_t>(b * kBN);
+        bool stop = false;
+        for (int i = 0; i < nkb; ++i) {
+          if (!dev::mbar_wait(full0 + 8 * s, ph & 1, abort_flag, p.dev_status,
+                              dev::kTimeoutMma)) {
+            stop = true;
+            break;
+          }
+          dev::tc_fence_after();
+          const uint32_t st = sbase + s * C::kStageBytes;
+          const uint32_t a_addr = kSwap ? st + C::kActBytes : st;
+          const uint32_t b_addr = kSwap ? st : st + C::kActBytes;
+          const uint64_t ad = dev::smem_desc_sw128(a_addr);
+          const uint64_t bd = dev::smem_desc_sw128(b_addr);
+#pragma unroll
+          for (int k = 0; k < kKBytes / 32; ++k)
+            dev::mma<kFp8>(d, ad + 2 * k, bd + 2 * k, idesc, (i | k) != 0);
+          dev::mma_commit(empty0 + 8 * s);
+          if (++s == stages) {
+            s = 0;
+            ++ph;
+          }
+        }
+        dev::mma_commit(tfull0 + 8 * b);
+        if (stop) break;
+      }
     }
-  } else if (warp == 1 && lane == 0) {
-    // ---------------------------------------------------------------- MMA
-    constexpr uint32_t idesc = dev::instr_desc(kFp8, kTile, kBN);
-    for (int i = 0; i < nkb; ++i) {
-      const int s = i % kStages;
-      const uint32_t ph = (i / kStages) & 1;
-      if (!dev::mbar_wait(full0 + 8 * s, ph, abort_flag, p.dev_status, dev::kTimeoutMma)) break;
+    __syncwarp();
+  } else {
+    // -------------------------------------------------------------- epilogue
+    const int et = threadIdx.x - 64;  // 0..127
+    const int ew = warp & 3;          // TMEM lane quarter of this warp
+    const int row = ew * 32 + lane;   // TMEM lane = tile row
+    const uint32_t lane_off = static_cast<uint32_t>(ew * 32) << 16;
+    uint8_t* wbuf = base + p.outbuf_off + (warp - 2) * 2 * kWarpOutBytes;  // this warp's 2 buffers
+    const uint32_t wbuf_s = sbase + p.outbuf_off + (warp - 2) * 2 * kWarpOutBytes;
+    int wb = 0;
+    bool ok = true;
+    for (int it = 0; it < my_tiles; ++it) {
+      int tm, tn;
+      tile_of(it, tm, tn);
+      const int b = it & 1;
+      const uint32_t u = static_cast<uint32_t>(it >> 1);
+      ok = dev::mbar_wait(tfull0 + 8 * b, u & 1, abort_flag, p.dev_status,
+                          dev::kTimeoutEpilogue);
+      ok = __all_sync(0xffffffffu, ok);
       dev::tc_fence_after();
-      const uint32_t st = sbase + s * C::kStageBytes;
-      const uint32_t a_addr = kSwap ? st + C::kActBytes : st;
-      const uint32_t b_addr = kSwap ? st : st + C::kActBytes;
-      const uint64_t ad = dev::smem_desc_sw128(a_addr);
-      const uint64_t bd = dev::smem_desc_sw128(b_addr);
-#pragma unroll
-      for (int k = 0; k < kKBytes / 32; ++k)
-        dev::mma<kFp8>(tmem, ad + 2 * k, bd + 2 * k, idesc, (i | k) != 0);
-      dev::mma_commit(empty0 + 8 * s);
-    }
-    dev::mma_commit(accum_bar);
-  }
-
-  // -------------------------------------------------------------------- epilogue
-  float* part = reinterpret_cast<float*>(base);  // split-K partial tile [col][lane]
-  bool ok = true;
-  const int ew = warp & 3;         // TMEM lane quarter of this warp
-  const int row = ew * 32 + lane;  // TMEM lane = tile row
-  if (warp >= 2) {
-    ok = dev::mbar_wait(accum_bar, 0, abort_flag, p.dev_status, dev::kTimeoutEpilogue);
-    ok = __all_sync(0xffffffffu, ok);
-    dev::tc_fence_after();
-    const uint32_t taddr = tmem + (static_cast<uint32_t>(ew * 32) << 16);
-    if (p.splits == 1) {
-      const float as = p.a_scale ? __ldg(p.a_scale) : 1.0f;
-      if constexpr (kSwap) {
-        const int n = tile_n * kTile + row;
-        const bool nvalid = ok && n < p.N;
-        float cs = 1.0f, b = 0.0f;
-        bool act = false;
-        if (nvalid) {
-          cs = as * (p.w_scale ? __ldg(p.w_scale + n) : 1.0f);
-          b = p.bias ? __ldg(p.bias + n) : 0.0f;
-          act = n < p.act_cols;
+      const uint32_t tacc = tmem + lane_off + static_cast<uint32_t>(b * kBN);
+      // the activation scale comes from the previous grid: read it only now
+      // (after the MMAs consumed activations loaded after the dependency
+      // wait) and through L2
+      const float as = p.a_scale ? __ldcg(p.a_scale) : 1.0f;
+      float* cs_s = col_sb + b * 2 * kBN;  // per-channel scale and bias of the tile
+      float* cb_s = cs_s + kBN;
+      float lcs = 1.0f, lcb = 0.0f;
+      bool lact = false;
+      if constexpr (!kSwap) {
+        for (int c = et; c < kBN; c += 128) {
+          const int n = tn * kBN + c;
+          cs_s[c] = n < p.N ? as * (p.w_scale ? __ldg(p.w_scale + n) : 1.0f) : 0.0f;
+          cb_s[c] = (n < p.N && p.bias) ? __ldg(p.bias + n) : 0.0f;
         }
-#pragma unroll 1
-        for (int c = 0; c < kBN / 32; ++c) {
-          float v[32];
-          dev::tmem_ld32(taddr + c * 32, v);
-          const int m0 = tile_m * kBN + c * 32;
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int m = m0 + j;
-            if (nvalid && m < p.M)
-              p.out[static_cast<int64_t>(m) * p.ldo + n] = __float2bfloat16_rn(epi(v[j], cs, b, act));
-          }
-        }
+        dev::named_sync(1, 128);
       } else {
-        const int m = tile_m * kTile + row;
-        const bool mvalid = ok && m < p.M;
+        const int n = tn * kTile + row;
+        if (n < p.N) {
+          lcs = as * (p.w_scale ? __ldg(p.w_scale + n) : 1.0f);
+          lcb = p.bias ? __ldg(p.bias + n) : 0.0f;
+          lact = n < p.act_cols;
+        }
+      }
+      // epilogue of 32 accumulator columns starting at tile column c32, and
+      // this warp's store of them
+      auto finish32 = [&](float* v, int c32, int rows_of_tile_m0) {
+        if constexpr (!kSwap) {
+          const int n0 = tn * kBN + c32;
+          const float4* cs4 = reinterpret_cast<const float4*>(cs_s + c32);
+          const float4* cb4 = reinterpret_cast<const float4*>(cb_s + c32);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const float4 sc = cs4[q];
+            const float4 bi = cb4[q];
+            v[4 * q + 0] = epi(v[4 * q + 0], sc.x, bi.x, n0 + 4 * q + 0 < p.act_cols);
+            v[4 * q + 1] = epi(v[4 * q + 1], sc.y, bi.y, n0 + 4 * q + 1 < p.act_cols);
+            v[4 * q + 2] = epi(v[4 * q + 2], sc.z, bi.z, n0 + 4 * q + 2 < p.act_cols);
+            v[4 * q + 3] = epi(v[4 * q + 3], sc.w, bi.w, n0 + 4 * q + 3 < p.act_cols);
+          }
+          warp_store<false, 32>(v, wbuf + wb * kWarpOutBytes, wbuf_s + wb * kWarpOutBytes,
+                                &tmap_out, n0, tm * kTile + ew * 32, lane);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = epi(v[j], lcs, lcb, lact);
+          warp_store<true, 32>(v, wbuf + wb * kWarpOutBytes, wbuf_s + wb * kWarpOutBytes,
+                               &tmap_out, tn * kTile + ew * 32, rows_of_tile_m0 + c32, lane);
+        }
+        wb ^= 1;
+      };
+
+      if (!split) {
+        if constexpr (kBN >= 64) {
 #pragma unroll 1
-        for (int c = 0; c < kBN / 32; ++c) {
-          float v[32];
-          dev::tmem_ld32(taddr + c * 32, v);
-          if (!mvalid) continue;
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int n = tile_n * kBN + c * 32 + q * 8;
-            if (n >= p.N) continue;
-            __align__(16) __nv_bfloat16 o[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const float cs = as * (p.w_scale ? __ldg(p.w_scale + n + e) : 1.0f);
-              const float b = p.bias ? __ldg(p.bias + n + e) : 0.0f;
-              o[e] = __float2bfloat16_rn(epi(v[q * 8 + e], cs, b, n + e < p.act_cols));
+          for (int c = 0; c < kBN; c += 64) {
+            float v[64];
+            dev::tmem_ld64(tacc + c, v);
+            if (c + 64 == kBN) {  // accumulator buffer free for the tile after next
+              dev::tc_fence_before();
+              __syncwarp();
+              if (lane == 0) dev::mbar_arrive(tempty0 + 8 * b);
             }
-            *reinterpret_cast<uint4*>(p.out + static_cast<int64_t>(m) * p.ldo + n) =
-                *reinterpret_cast<const uint4*>(o);
+            finish32(v, c, tm * kBN);
+            finish32(v + 32, c + 32, tm * kBN);
           }
-        }
-      }
-    } else {
-      // split-K: this CTA's fp32 partial tile -> own shared memory, [col][lane]
-#pragma unroll 1
-      for (int c = 0; c < kBN / 32; ++c) {
-        float v[32];
-        dev::tmem_ld32(taddr + c * 32, v);
-#pragma unroll
-        for (int j = 0; j < 32; ++j) part[(c * 32 + j) * kPitch + row] = v[j];
-      }
-    }
-  }
-
-  __syncwarp();
-  if (p.splits > 1) {
-    dev::cluster_sync();  // every partial tile of the cluster is written
-    if (warp >= 2) {
-      const uint32_t rank = dev::cluster_ctarank();
-      const int S = p.splits;
-      const float as = p.a_scale ? __ldg(p.a_scale) : 1.0f;
-      const uint32_t part_s = dev::smem_u32(part);
-      if constexpr (kSwap) {
-        // columns = activation rows m; each CTA reduces a slice of them
-        const int cpr = (kBN + S - 1) / S;
-        const int c0 = rank * cpr;
-        const int c1 = min(kBN, c0 + cpr);
-        const int n = tile_n * kTile + row;
-        const bool nvalid = ok && n < p.N;
-        float cs = 1.0f, b = 0.0f;
-        bool act = false;
-        if (nvalid) {
-          cs = as * (p.w_scale ? __ldg(p.w_scale + n) : 1.0f);
-          b = p.bias ? __ldg(p.bias + n) : 0.0f;
-          act = n < p.act_cols;
-        }
-        for (int c = c0; c < c1; ++c) {
-          const int m = tile_m * kBN + c;
-          if (!nvalid || m >= p.M) continue;
-          const uint32_t off = part_s + static_cast<uint32_t>((c * kPitch + row) * 4);
-          float acc = 0.0f;
-          for (int s = 0; s < S; ++s) acc += dev::ld_dsmem_f32(dev::map_to_rank(off, s));
-          p.out[static_cast<int64_t>(m) * p.ldo + n] = __float2bfloat16_rn(epi(acc, cs, b, act));
+        } else {
+          float v[32];
+          dev::tmem_ld32(tacc, v);
+          dev::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) dev::mbar_arrive(tempty0 + 8 * b);
+          finish32(v, 0, tm * kBN);
         }
       } else {
-        // lanes = activation rows m; each CTA reduces a slice of rows, its
-        // 128 epilogue threads walk the columns (coalesced stores)
-        const int t = threadIdx.x - 64;
-        const int rpr = (kTile + S - 1) / S;
-        const int r0 = rank * rpr;
-        const int r1 = min(kTile, r0 + rpr);
-        for (int r = r0; r < r1; ++r) {
-          const int m = tile_m * kTile + r;
-          if (!ok || m >= p.M) break;
-          for (int c = t; c < kBN; c += 128) {
-            const int n = tile_n * kBN + c;
-            if (n >= p.N) continue;
-            const uint32_t off = part_s + static_cast<uint32_t>((c * kPitch + r) * 4);
-            float acc = 0.0f;
-            for (int s = 0; s < S; ++s) acc += dev::ld_dsmem_f32(dev::map_to_rank(off, s));
-            const float cs = as * (p.w_scale ? __ldg(p.w_scale + n) : 1.0f);
-            const float b = p.bias ? __ldg(p.bias + n) : 0.0f;
-            p.out[static_cast<int64_t>(m) * p.ldo + n] =
-                __float2bfloat16_rn(epi(acc, cs, b, n < p.act_cols));
+        // ------------- split-K: exchange partial chunks inside the cluster
+        const int owned = own_c1 - own_c0;
+        if (p.recv_in_stages) dev::cluster_arrive();  // this CTA's stage buffers are free
+        // 1. the chunks other ranks own -> this CTA's send buffer (stage region)
+        for (int c = 0; c < NC; ++c) {
+          if (c >= own_c0 && c < own_c1) continue;
+          const int sp = c < own_c0 ? c : c - owned;  // position in the send buffer
+          uint8_t* dst = base + sp * chunk_bytes;
+          if (CW == 32) {
+            float v[32];
+            dev::tmem_ld32(tacc + c * 32, v);
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              *reinterpret_cast<float4*>(dst + chunk_off(row, q, 32)) =
+                  make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+          } else {
+            float v[8];
+            dev::tmem_ld8(tacc + c * 8, v);
+            *reinterpret_cast<float4*>(dst + chunk_off(row, 0, 8)) =
+                make_float4(v[0], v[1], v[2], v[3]);
+            *reinterpret_cast<float4*>(dst + chunk_off(row, 1, 8)) =
+                make_float4(v[4], v[5], v[6], v[7]);
+          }
+        }
+        dev::fence_proxy_async_smem();
+        dev::named_sync(1, 128);
+        // 2. after phase 1 (every peer initialised and its receive buffer
+        //    free), one bulk copy per owner
+        dev::cluster_wait();
+        if (et == 0) {
+          for (int o = 0; o < S; ++o) {
+            if (o == rank) continue;
+            const int oc0 = chunk_begin(o), oc1 = chunk_begin(o + 1);
+            const int sp0 = oc0 < own_c0 ? oc0 : oc0 - owned;
+            const int slot = rank < o ? rank : rank - 1;
+            const uint32_t dst = dev::map_to_rank(
+                sbase + p.recv_off + static_cast<uint32_t>(slot * owned_max) * chunk_bytes, o);
+            dev::bulk_copy_to_peer(dst, sbase + sp0 * chunk_bytes,
+                                   static_cast<uint32_t>(oc1 - oc0) * chunk_bytes,
+                                   dev::map_to_rank(recv_bar, o));
+          }
+        }
+        // 3. own chunks: own partial + received partials, in rank order
+        ok = dev::mbar_wait(recv_bar, 0, abort_flag, p.dev_status, dev::kTimeoutEpilogue) && ok;
+        ok = __all_sync(0xffffffffu, ok);
+        dev::cluster_arrive();  // phase 2: every copy into this CTA has landed
+        const uint8_t* recv = base + p.recv_off;
+        for (int c = own_c0; c < own_c1; ++c) {
+          const int lc = c - own_c0;
+          float acc[32];
+          if (CW == 32) {
+            dev::tmem_ld32(tacc + c * 32, acc);
+          } else {
+            float w8[8];
+            dev::tmem_ld8(tacc + c * 8, w8);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc[j] = w8[j];
+#pragma unroll
+            for (int j = 8; j < 32; ++j) acc[j] = 0.0f;
+          }
+          // partial sums added in rank order, this CTA's own at its rank
+          float sum[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) sum[j] = 0.0f;
+          for (int r = 0; r < S; ++r) {
+            if (r == rank) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) sum[j] += acc[j];
+            } else {
+              const int slot = r < rank ? r : r - 1;
+              const uint8_t* src = recv + (slot * owned_max + lc) * chunk_bytes;
+#pragma unroll
+              for (int q = 0; q < 8; ++q) {
+                if (4 * q < CW) {
+                  const float4 x = *reinterpret_cast<const float4*>(src + chunk_off(row, q, CW));
+                  sum[4 * q] += x.x;
+                  sum[4 * q + 1] += x.y;
+                  sum[4 * q + 2] += x.z;
+                  sum[4 * q + 3] += x.w;
+                }
+              }
+            }
+          }
+          if constexpr (!kSwap) {
+            finish32(sum, c * 32, 0);
+          } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) sum[j] = epi(sum[j], lcs, lcb, lact);
+            warp_store<true, 8>(sum, wbuf + wb * kWarpOutBytes, wbuf_s + wb * kWarpOutBytes,
+                                &tmap_out, tn * kTile + ew * 32, tm * kBN + c * 8, lane);
+            wb ^= 1;
           }
         }
       }
+      if (!ok) break;
     }
-    dev::cluster_sync();  // no CTA leaves while a peer still reads its tile
+    if (lane == 0) dev::bulk_wait_all();  // stores complete before the grid ends
   }
 
+  if (split) {
+    if (warp < 2) {  // the copy and MMA warps: both barrier phases
+      if (p.recv_in_stages) dev::cluster_arrive();
+      dev::cluster_wait();
+      dev::cluster_arrive();
+    }
+    // phase 2: every CTA has received its chunks, so no copy out of this
+    // CTA's shared memory is still in flight
+    dev::cluster_wait();
+  }
   dev::tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -341,50 +579,140 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
+// Static per-shape choices (frozen at call time; the same shape always gets
+// the same plan): tile kind and width, split-K factor, grid, pipeline depth.
 struct Plan {
   bool swap;
   int bn;
+  int tiles_m, tiles_n, num_tiles;
   int splits;
   int kb_per_split;
+  int chunk_cols;
+  int stages;
+  bool recv_in_stages;
+  int outbuf_off, recv_off, tail_off;
+  int smem;
   dim3 grid;
 };
+
+// Shared-memory layout for a given depth; false if it does not fit.
+bool layout(Plan& pl, int stage_bytes) {
+  const int pipe = pl.stages * stage_bytes;
+  pl.outbuf_off = pipe;
+  pl.recv_off = 0;
+  int tail = pipe + kOutBytes;
+  if (pl.splits > 1) {
+    const int nchunks = pl.bn / pl.chunk_cols;
+    const int chunk = kTile * pl.chunk_cols * 4;
+    const int owned_max = static_cast<int>(ceil_div(nchunks, pl.splits));
+    const int owned_min = nchunks / pl.splits;
+    const int recv = (pl.splits - 1) * owned_max * chunk;
+    const int send = (nchunks - owned_min) * chunk;
+    if (send > pipe) return false;
+    if (!pl.recv_in_stages) {
+      pl.recv_off = tail;
+      tail += recv;
+    } else {
+      pl.recv_off = send;
+      if (send + recv > pipe) return false;
+    }
+  }
+  pl.tail_off = static_cast<int>(ceil_div(tail, 128) * 128);
+  pl.smem = 1024 + pl.tail_off + 16 * pl.bn + kBarRegion;
+  return pl.smem <= kSmemMax;
+}
 
 Plan make_plan(int64_t M, int64_t N, int64_t K, int esize) {
   Plan pl;
   const int kb = static_cast<int>(ceil_div(K * esize, kKBytes));
   const int nb = static_cast<int>(ceil_div(N, kTile));
-  int tiles;
   if (M <= 128) {
     pl.swap = true;
     pl.bn = M <= 32 ? 32 : (M <= 64 ? 64 : 128);
-    tiles = nb * static_cast<int>(ceil_div(M, pl.bn));
+    pl.tiles_n = nb;
+    pl.tiles_m = static_cast<int>(ceil_div(M, pl.bn));
+    pl.chunk_cols = 8;
   } else {
     pl.swap = false;
     pl.bn = 256;
-    tiles = static_cast<int>(ceil_div(N, 256) * ceil_div(M, kTile));
+    pl.tiles_m = static_cast<int>(ceil_div(M, kTile));
+    pl.tiles_n = static_cast<int>(ceil_div(N, 256));
+    pl.chunk_cols = 32;
   }
+  pl.num_tiles = pl.tiles_m * pl.tiles_n;
   const int sms = sm_count() > 0 ? sm_count() : 148;
   int s = 1;
-  if (tiles < sms) {
-    s = sms / tiles;
+  if (pl.num_tiles < sms) {
+    s = sms / pl.num_tiles;
+    const int nchunks = pl.bn / pl.chunk_cols;
     if (s > kMaxSplits) s = kMaxSplits;
+    if (s > nchunks) s = nchunks;
     if (s > kb) s = kb;
     if (s < 1) s = 1;
   }
   pl.kb_per_split = static_cast<int>(ceil_div(kb, s));
   pl.splits = static_cast<int>(ceil_div(kb, pl.kb_per_split));
-  if (pl.swap)
-    pl.grid = dim3(nb, static_cast<unsigned>(ceil_div(M, pl.bn)), pl.splits);
+  const int act_rows = pl.swap ? pl.bn : kTile;
+  const int w_rows = pl.swap ? kTile : pl.bn;
+  const int stage_bytes = (act_rows + w_rows) * kKBytes;
+  // pipeline depth: small M takes just the CTA's k-blocks (a small footprint
+  // lets a dependent grid's CTAs be resident early and prefetch); large M
+  // and multi-tile walks take as many as fit
+  int want = kMaxStages;
+  if (pl.swap) {
+    const int per_cta = pl.splits > 1 ? pl.kb_per_split : kb;
+    want = per_cta < 2 ? 2 : (per_cta > kMaxStages ? kMaxStages : per_cta);
+    if (pl.splits == 1 && pl.num_tiles > sms) want = kMaxStages;
+  }
+  // split-K receive buffers: a dedicated region (no barrier after the
+  // mainloop) or inside the stage buffers, whichever leaves the deeper
+  // pipeline (dedicated on a tie)
+  bool placed = false;
+  int best_st = 0;
+  bool best_in_stages = false;
+  for (int mode = 0; mode < (pl.splits > 1 ? 2 : 1); ++mode) {
+    pl.recv_in_stages = mode == 1;
+    for (int st = kMaxStages; st >= 2; --st) {
+      if (st > want && !(pl.recv_in_stages && st <= kMaxStages)) continue;
+      pl.stages = st;
+      if (layout(pl, stage_bytes)) {
+        // a receive region inside the stages may need more depth than wanted
+        const int eff = st > want ? want : st;
+        if (!placed || eff > best_st) {
+          placed = true;
+          best_st = eff;
+          best_in_stages = pl.recv_in_stages;
+        }
+        break;
+      }
+    }
+  }
+  if (placed) {
+    pl.recv_in_stages = best_in_stages;
+    for (int st = best_in_stages ? kMaxStages : want; st >= 2; --st) {
+      pl.stages = st;
+      if (layout(pl, stage_bytes)) break;
+    }
+  }
+  if (!placed) {  // no split fits: run unsplit
+    pl.splits = 1;
+    pl.kb_per_split = kb;
+    pl.recv_in_stages = false;
+    for (int st = kMaxStages; st >= 2 && !placed; --st) {
+      pl.stages = st;
+      placed = layout(pl, stage_bytes);
+    }
+  }
+  if (pl.splits > 1)
+    pl.grid = dim3(static_cast<unsigned>(pl.num_tiles), 1, static_cast<unsigned>(pl.splits));
   else
-    pl.grid = dim3(static_cast<unsigned>(ceil_div(N, 256)), static_cast<unsigned>(ceil_div(M, kTile)),
-                   pl.splits);
+    pl.grid = dim3(static_cast<unsigned>(pl.num_tiles < sms ? pl.num_tiles : sms), 1, 1);
   return pl;
 }
 
 template <bool kFp8, bool kSwap, int kBN>
-cudaError_t launch_one(const CUtensorMap& tm, const GemmArgs& a, const Plan& pl,
-                       cudaStream_t stream) {
-  using C = Cfg<kSwap, kBN>;
+cudaError_t launch_one(const CUtensorMap& ta, const CUtensorMap& to, const GemmArgs& a,
+                       const Plan& pl, cudaStream_t stream) {
   auto kern = gemm_tc_kernel<kFp8, kSwap, kBN>;
   static std::mutex mu;
   static bool attr_set[64] = {false};
@@ -394,7 +722,7 @@ cudaError_t launch_one(const CUtensorMap& tm, const GemmArgs& a, const Plan& pl,
     std::lock_guard<std::mutex> lock(mu);
     if (dev >= 0 && dev < 64 && !attr_set[dev]) {
       cudaError_t e =
-          cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+          cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
       if (e != cudaSuccess) return e;
       attr_set[dev] = true;
     }
@@ -402,26 +730,28 @@ cudaError_t launch_one(const CUtensorMap& tm, const GemmArgs& a, const Plan& pl,
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = pl.grid;
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.dynamicSmemBytes = pl.smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 1;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = pl.splits;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = 1;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = pl.splits;
   cfg.attrs = attr;
-  cfg.numAttrs = pl.splits > 1 ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, kern, tm, a);
+  cfg.numAttrs = pl.splits > 1 ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, kern, ta, to, a);
 }
 
 template <bool kFp8>
-cudaError_t dispatch(const CUtensorMap& tm, const GemmArgs& a, const Plan& pl,
-                     cudaStream_t stream) {
-  if (!pl.swap) return launch_one<kFp8, false, 256>(tm, a, pl, stream);
+cudaError_t dispatch(const CUtensorMap& ta, const CUtensorMap& to, const GemmArgs& a,
+                     const Plan& pl, cudaStream_t stream) {
+  if (!pl.swap) return launch_one<kFp8, false, 256>(ta, to, a, pl, stream);
   switch (pl.bn) {
-    case 32: return launch_one<kFp8, true, 32>(tm, a, pl, stream);
-    case 64: return launch_one<kFp8, true, 64>(tm, a, pl, stream);
-    default: return launch_one<kFp8, true, 128>(tm, a, pl, stream);
+    case 32: return launch_one<kFp8, true, 32>(ta, to, a, pl, stream);
+    case 64: return launch_one<kFp8, true, 64>(ta, to, a, pl, stream);
+    default: return launch_one<kFp8, true, 128>(ta, to, a, pl, stream);
   }
 }
 
@@ -450,25 +780,37 @@ frt_status gemm_common(bool fp8, const void* a, int64_t lda, const float* a_scal
   if (!encode) return FRT_ERR_CUDA;
   const Plan pl = make_plan(M, N, K, esize);
 
-  CUtensorMap tm;
-  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(lda * esize)};
-  const cuuint32_t box[2] = {static_cast<cuuint32_t>(kKBytes / esize),
-                             static_cast<cuuint32_t>(pl.swap ? pl.bn : kTile)};
-  const cuuint32_t estr[2] = {1, 1};
-  CUresult r = encode(&tm, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
-                      2, const_cast<void*>(a), dims, strides, box, estr,
-                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return FRT_ERR_CUDA;
+  CUtensorMap ta, to;
+  {
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(lda * esize)};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kKBytes / esize),
+                               static_cast<cuuint32_t>(pl.swap ? pl.bn : kTile)};
+    const cuuint32_t estr[2] = {1, 1};
+    if (encode(&ta, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+               const_cast<void*>(a), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return FRT_ERR_CUDA;
+  }
+  {
+    // output boxes, one per epilogue warp and chunk: {32 channels, 32 rows}
+    // (small M split-K: {32 channels, 8 rows}), 64-byte swizzle
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(M)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ldo * 2)};
+    const cuuint32_t box[2] = {32u, (pl.swap && pl.splits > 1) ? 8u : 32u};
+    const cuuint32_t estr[2] = {1, 1};
+    if (encode(&to, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, out, dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+               CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return FRT_ERR_CUDA;
+  }
 
   GemmArgs ga;
   ga.w_packed = static_cast<const uint8_t*>(w_packed);
   ga.a_scale = a_scale;
   ga.w_scale = w_scale;
   ga.bias = bias;
-  ga.out = static_cast<__nv_bfloat16*>(out);
-  ga.ldo = ldo;
   ga.M = static_cast<int>(M);
   ga.N = static_cast<int>(N);
   ga.act_cols = act == FRT_ACT_GELU_TANH ? static_cast<int>(act_cols) : 0;
@@ -476,10 +818,19 @@ frt_status gemm_common(bool fp8, const void* a, int64_t lda, const float* a_scal
   ga.nb_total = static_cast<int>(ceil_div(N, kTile));
   ga.kb_per_split = pl.kb_per_split;
   ga.splits = pl.splits;
+  ga.tiles_m = pl.tiles_m;
+  ga.tiles_n = pl.tiles_n;
+  ga.num_tiles = pl.num_tiles;
+  ga.stages = pl.stages;
+  ga.chunk_cols = pl.chunk_cols;
+  ga.recv_in_stages = pl.recv_in_stages ? 1 : 0;
+  ga.outbuf_off = pl.outbuf_off;
+  ga.recv_off = pl.recv_off;
+  ga.tail_off = pl.tail_off;
   ga.dev_status = dev_status;
 
-  cudaError_t e = fp8 ? dispatch<true>(tm, ga, pl, as_cuda(stream))
-                      : dispatch<false>(tm, ga, pl, as_cuda(stream));
+  cudaError_t e = fp8 ? dispatch<true>(ta, to, ga, pl, as_cuda(stream))
+                      : dispatch<false>(ta, to, ga, pl, as_cuda(stream));
   if (e != cudaSuccess) {
     cudaGetLastError();
     return FRT_ERR_CUDA;

@@ -100,7 +100,11 @@ def frt_packed_weight_bytes(K, N, packed_dtype="e4m3"):
 
 def frt_pack_weights(w, packed_dtype="e4m3", packed=None, stream=None):
     """Packs W [K x N] (uint8 OCP E4M3 bytes for 'e4m3'; fp32 or bf16 for
-    'bf16') into the kernels' tile layout; returns the uint8 buffer."""
+    'bf16') into the kernels' tile layout; returns the uint8 buffer.
+
+    Load-time: a GEMM fetches its weight tiles before waiting for the kernel
+    launched just before it, so synchronise (or launch another kernel)
+    between packing and the first GEMM that reads the result."""
     K, N, ldw = _rows_view(w, "w")
     if packed_dtype == "e4m3":
         if w.dtype != torch.uint8:

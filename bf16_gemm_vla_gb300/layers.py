@@ -42,13 +42,17 @@ def prepare_fp8(w_f32, bias=None, import_fnuz=False):
     if import_fnuz:
         frt.frt_fnuz_to_ocp(q.view(-1), out=q.view(-1))
     packed = frt.frt_pack_weights(q, "e4m3")
+    # packed weights are load-time data: complete before any GEMM reads them
+    torch.cuda.current_stream(packed.device).synchronize()
     return PackedWeight(packed, K, N, "e4m3", s, bias)
 
 
 def prepare_bf16(w, bias=None):
     """Round W (fp32 or bf16) to bf16 and pack it."""
     K, N = w.shape
-    return PackedWeight(frt.frt_pack_weights(w, "bf16"), K, N, "bf16", None, bias)
+    packed = frt.frt_pack_weights(w, "bf16")
+    torch.cuda.current_stream(packed.device).synchronize()
+    return PackedWeight(packed, K, N, "bf16", None, bias)
 
 
 class Linear:

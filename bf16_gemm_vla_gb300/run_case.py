@@ -1,0 +1,66 @@
+"""Runs one layer of the path a few times, for profiling (e.g. under ncu).
+
+    python -m bf16_gemm_vla_gb300.run_case --kind fp8 --M 50 --K 1024 --N 4096 --reps 3
+
+Synthetic inputs are drawn on the device (seeded): activations N(0,1) bf16,
+weights N(0,0.02), bias N(0,0.1).  The FP8 path quantizes the activations
+per tensor and the weights per output channel (load time, before the timed
+launches), then launches the GEMM `reps` times; --with-quantize repeats the
+activation quantize before each GEMM.  Prints the mean device time per
+launch (CUDA events) unless --quiet.
+"""
+import argparse
+
+import torch
+
+from . import frt, layers
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--kind", choices=("fp8", "bf16"), default="fp8")
+    ap.add_argument("--M", type=int, default=50)
+    ap.add_argument("--K", type=int, default=1024)
+    ap.add_argument("--N", type=int, default=4096)
+    ap.add_argument("--act-cols", type=int, default=0)
+    ap.add_argument("--reps", type=int, default=3)
+    ap.add_argument("--with-quantize", action="store_true")
+    ap.add_argument("--quiet", action="store_true")
+    a = ap.parse_args(argv)
+    dev = torch.device("cuda")
+    g = torch.Generator(device=dev)
+    g.manual_seed(0)
+    x = torch.randn((a.M, a.K), generator=g, device=dev).to(torch.bfloat16)
+    w = torch.randn((a.K, a.N), generator=g, device=dev) * 0.02
+    b = torch.randn((a.N,), generator=g, device=dev) * 0.1
+    pw = layers.prepare_fp8(w, b) if a.kind == "fp8" else layers.prepare_bf16(w, b)
+    lin = layers.Linear(pw, a.M, act_cols=a.act_cols)
+    if a.kind == "fp8":
+        frt.frt_quantize_e4m3(x, frt.PER_TENSOR, frt.OCP, q=lin.q, scale=lin.a_scale,
+                              workspace=lin.ws)
+
+    def once():
+        if a.kind == "fp8":
+            if a.with_quantize:
+                return lin(x)
+            return frt.frt_gemm_fp8(lin.q, lin.a_scale, pw.packed, pw.w_scale, pw.N, bias=b,
+                                    act_cols=a.act_cols, out=lin.out)
+        return lin(x)
+
+    once()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(a.reps):
+        once()
+    e1.record()
+    torch.cuda.synchronize()
+    frt.check_device_status()
+    if not a.quiet:
+        print("%s M=%d K=%d N=%d: %.2f us per launch" % (a.kind, a.M, a.K, a.N,
+                                                          e0.elapsed_time(e1) * 1e3 / a.reps))
+
+
+if __name__ == "__main__":
+    main()

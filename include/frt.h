@@ -173,6 +173,13 @@ frt_status frt_pack_weights(const void* w, frt_dtype w_dtype, int64_t K, int64_t
  * a_scale   : device, 1 float (the activation's per-tensor dequant scale).
  * w_packed  : from frt_pack_weights with the same K and N (FRT_E4M3_OCP for
  *             frt_gemm_fp8, FRT_BF16 for frt_gemm_bf16); 16-byte aligned.
+ *             Load-time data: the kernel starts fetching weight tiles before
+ *             it waits for the previous kernel on the stream (programmatic
+ *             dependent launch), so w_packed must be complete before that
+ *             previous kernel started (pack at load time and synchronise, or
+ *             leave at least one other kernel between the pack and the GEMM).
+ *             Everything else (a, a_scale, w_scale, bias, out) may come from
+ *             the previous kernel.
  * w_scale   : device, N floats (per output channel); NULL means 1.
  *             Required (non-NULL) for frt_gemm_fp8.
  * bias      : device, N floats; NULL means 0.

@@ -69,6 +69,7 @@ def fp8_layer(lay, import_fnuz=False, act_cols=None, bias=True):
         qw_o = convert.fnuz_to_ocp(qw_o)
         np.testing.assert_array_equal(qw.cpu().numpy(), qw_o)
     wp = frt.frt_pack_weights(qw, "e4m3")
+    torch.cuda.synchronize()  # packed weights are load-time data
     out = frt.frt_gemm_fp8(qa, sa, wp, sw, N, bias=b_dev, act_cols=act_cols)
     frt.check_device_status()
     y, sumabs = gemm.gemm_fp8(qa_o, e4m3.OCP, sa_o, qw_o, e4m3.OCP, sw_o,
@@ -85,6 +86,7 @@ def bf16_layer(lay, act_cols=None, bias=True, w_scale=None):
     wp = frt.frt_pack_weights(torch.from_numpy(lay["w_f32"]).cuda(), "bf16")
     b_dev = torch.from_numpy(lay["bias"]).cuda() if bias else None
     ws_dev = None if w_scale is None else torch.from_numpy(w_scale).cuda()
+    torch.cuda.synchronize()  # packed weights are load-time data
     out = frt.frt_gemm_bf16(a_dev, wp, N, w_scale=ws_dev, bias=b_dev, act_cols=act_cols)
     frt.check_device_status()
     w_bf = obf16.round_to_bf16(lay["w_f32"])
@@ -122,9 +124,11 @@ def test_integer_gemm_exact():
         qw, _ = frt.frt_quantize_e4m3(torch.from_numpy(w).cuda(), frt.PER_COL, frt.OCP,
                                       static_scale=torch.ones(N, device="cuda"))
         wp = frt.frt_pack_weights(qw, "e4m3")
+        torch.cuda.synchronize()  # packed weights are load-time data
         out = frt.frt_gemm_fp8(qa, one, wp, torch.ones(N, device="cuda"), N)
         np.testing.assert_array_equal(out.float().cpu().numpy(), exact.astype(np.float32))
         wb = frt.frt_pack_weights(torch.from_numpy(w).cuda(), "bf16")
+        torch.cuda.synchronize()
         out = frt.frt_gemm_bf16(torch.from_numpy(a).cuda().to(torch.bfloat16), wb, N)
         np.testing.assert_array_equal(out.float().cpu().numpy(), exact.astype(np.float32))
         frt.check_device_status()
@@ -184,6 +188,7 @@ def test_strided_activations_and_output():
     a_f32 = big.float().cpu().numpy()[:, :1024]
     wp = frt.frt_pack_weights(torch.from_numpy(lay["w_f32"]).cuda(), "bf16")
     out_big = torch.zeros((50, 640), dtype=torch.bfloat16, device="cuda")
+    torch.cuda.synchronize()
     frt.frt_gemm_bf16(a, wp, 512, bias=torch.from_numpy(lay["bias"]).cuda(),
                       out=out_big[:, :512])
     y, sumabs = gemm.gemm_bf16(a_f32, obf16.round_to_bf16(lay["w_f32"]), None, lay["bias"], 0)
