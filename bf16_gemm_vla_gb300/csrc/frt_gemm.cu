@@ -96,16 +96,17 @@ struct Cfg {
   static_assert(kSwap || kBN == 256, "large-M tiles are 128 x 256");
 };
 
+// tanh-GELU, 0.5 v (1 + tanh(u)) with u = sqrt(2/pi) (v + 0.044715 v^3),
+// evaluated through the identity 0.5 (1 + tanh(u)) = 1 / (1 + exp(-2u)):
+// the relative error stays near 1e-6 even where 1 + tanh(u) cancels
+// (large negative v), and exp(-2u) -> inf gives the limit 0.
 __device__ __forceinline__ float gelu_tanh(float v) {
-  const float k0 = 0.7978845608028654f;  // sqrt(2 / pi)
-  const float u = k0 * (v + 0.044715f * v * v * v);
-  return 0.5f * v * (1.0f + tanhf(u));
+  const float k2 = 1.5957691216057308f;  // 2 sqrt(2 / pi)
+  const float t = k2 * fmaf(0.044715f * v, v * v, v);
+  return __fdividef(v, 1.0f + __expf(-t));
 }
 
-__device__ __forceinline__ float epi(float acc, float cs, float b, bool act) {
-  const float v = fmaf(acc, cs, b);
-  return act ? gelu_tanh(v) : v;
-}
+__device__ __forceinline__ float lin(float acc, float cs, float b) { return fmaf(acc, cs, b); }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
@@ -407,16 +408,25 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int q = 0; q < 8; ++q) {
             const float4 sc = cs4[q];
             const float4 bi = cb4[q];
-            v[4 * q + 0] = epi(v[4 * q + 0], sc.x, bi.x, n0 + 4 * q + 0 < p.act_cols);
-            v[4 * q + 1] = epi(v[4 * q + 1], sc.y, bi.y, n0 + 4 * q + 1 < p.act_cols);
-            v[4 * q + 2] = epi(v[4 * q + 2], sc.z, bi.z, n0 + 4 * q + 2 < p.act_cols);
-            v[4 * q + 3] = epi(v[4 * q + 3], sc.w, bi.w, n0 + 4 * q + 3 < p.act_cols);
+            v[4 * q + 0] = lin(v[4 * q + 0], sc.x, bi.x);
+            v[4 * q + 1] = lin(v[4 * q + 1], sc.y, bi.y);
+            v[4 * q + 2] = lin(v[4 * q + 2], sc.z, bi.z);
+            v[4 * q + 3] = lin(v[4 * q + 3], sc.w, bi.w);
+          }
+          if (n0 < p.act_cols) {  // uniform across the warp: the chunk's columns
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (n0 + j < p.act_cols) v[j] = gelu_tanh(v[j]);
           }
           warp_store<false, 32>(v, wbuf + wb * kWarpOutBytes, wbuf_s + wb * kWarpOutBytes,
                                 &tmap_out, n0, tm * kTile + ew * 32, lane);
         } else {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] = epi(v[j], lcs, lcb, lact);
+          for (int j = 0; j < 32; ++j) v[j] = lin(v[j], lcs, lcb);
+          if (lact) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = gelu_tanh(v[j]);
+          }
           warp_store<true, 32>(v, wbuf + wb * kWarpOutBytes, wbuf_s + wb * kWarpOutBytes,
                                &tmap_out, tn * kTile + ew * 32, rows_of_tile_m0 + c32, lane);
         }
@@ -533,7 +543,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             finish32(sum, c * 32, 0);
           } else {
 #pragma unroll
-            for (int j = 0; j < 8; ++j) sum[j] = epi(sum[j], lcs, lcb, lact);
+            for (int j = 0; j < 8; ++j) sum[j] = lin(sum[j], lcs, lcb);
+            if (lact) {
+#pragma unroll
+              for (int j = 0; j < 8; ++j) sum[j] = gelu_tanh(sum[j]);
+            }
             warp_store<true, 8>(sum, wbuf + wb * kWarpOutBytes, wbuf_s + wb * kWarpOutBytes,
                                 &tmap_out, tn * kTile + ew * 32, tm * kBN + c * 8, lane);
             wb ^= 1;
@@ -622,7 +636,109 @@ bool layout(Plan& pl, int stage_bytes) {
   return pl.smem <= kSmemMax;
 }
 
-Plan make_plan(int64_t M, int64_t N, int64_t K, int esize) {
+// Sets the kernel's dynamic shared memory limit once per device.
+template <bool kFp8, bool kSwap, int kBN>
+cudaError_t prepare_kernel() {
+  static std::mutex mu;
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<kFp8, kSwap, kBN>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  return cudaSuccess;
+}
+
+// Number of clusters of `s` CTAs with `smem` bytes each that can be resident
+// at once (cached per device and configuration).
+template <bool kFp8, bool kSwap, int kBN>
+int cluster_capacity(int s, int smem) {
+  static std::mutex mu;
+  static int cache[64][kMaxSplits + 1][8];
+  static bool init = false;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (prepare_kernel<kFp8, kSwap, kBN>() != cudaSuccess) return 0;
+  const int sb = (smem + 32767) / 32768;  // smem bucket of 32 KiB
+  std::lock_guard<std::mutex> lock(mu);
+  if (!init) {
+    for (auto& a : cache)
+      for (auto& b : a)
+        for (int& c : b) c = -1;
+    init = true;
+  }
+  int& c = cache[dev][s][sb < 8 ? sb : 7];
+  if (c < 0) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1, 1, static_cast<unsigned>(s));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = static_cast<size_t>(sb < 8 ? sb * 32768 : kSmemMax);
+    if (cfg.dynamicSmemBytes > static_cast<size_t>(kSmemMax)) cfg.dynamicSmemBytes = kSmemMax;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = static_cast<unsigned>(s);
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<kFp8, kSwap, kBN>, &cfg) != cudaSuccess) {
+      cudaGetLastError();
+      n = 0;
+    }
+    c = n;
+  }
+  return c;
+}
+
+template <bool kFp8>
+int cluster_capacity_for(bool swap, int bn, int s, int smem) {
+  if (!swap) return cluster_capacity<kFp8, false, 256>(s, smem);
+  switch (bn) {
+    case 32: return cluster_capacity<kFp8, true, 32>(s, smem);
+    case 64: return cluster_capacity<kFp8, true, 64>(s, smem);
+    default: return cluster_capacity<kFp8, true, 128>(s, smem);
+  }
+}
+
+// Places the pipeline and the split-K receive buffers: the deepest pipeline
+// (up to `want` stages) with a dedicated receive region, or with the
+// receive buffers inside the stage buffers if that allows a deeper one.
+bool place_buffers(Plan& pl, int stage_bytes, int want) {
+  int best = 0;
+  bool best_in_stages = false;
+  for (int mode = 0; mode < (pl.splits > 1 ? 2 : 1); ++mode) {
+    pl.recv_in_stages = mode == 1;
+    for (int st = kMaxStages; st >= 2; --st) {
+      if (!pl.recv_in_stages && st > want) continue;
+      pl.stages = st;
+      if (!layout(pl, stage_bytes)) continue;
+      const int eff = st < want ? st : want;
+      if (eff > best) {
+        best = eff;
+        best_in_stages = pl.recv_in_stages;
+      }
+      break;
+    }
+  }
+  if (best == 0) return false;
+  pl.recv_in_stages = best_in_stages;
+  for (int st = best_in_stages ? kMaxStages : want; st >= 2; --st) {
+    pl.stages = st;
+    if (layout(pl, stage_bytes)) return true;
+  }
+  return false;
+}
+
+// Static per-shape choices (the same shape always gets the same plan): tile
+// kind and width, split-K factor, grid and pipeline depth.  The split is the
+// largest one that fits shared memory and keeps every cluster resident in
+// one wave.
+Plan make_plan(int64_t M, int64_t N, int64_t K, int esize, bool fp8) {
   Plan pl;
   const int kb = static_cast<int>(ceil_div(K * esize, kKBytes));
   const int nb = static_cast<int>(ceil_div(N, kTile));
@@ -641,67 +757,36 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int esize) {
   }
   pl.num_tiles = pl.tiles_m * pl.tiles_n;
   const int sms = sm_count() > 0 ? sm_count() : 148;
-  int s = 1;
-  if (pl.num_tiles < sms) {
-    s = sms / pl.num_tiles;
-    const int nchunks = pl.bn / pl.chunk_cols;
-    if (s > kMaxSplits) s = kMaxSplits;
-    if (s > nchunks) s = nchunks;
-    if (s > kb) s = kb;
-    if (s < 1) s = 1;
-  }
-  pl.kb_per_split = static_cast<int>(ceil_div(kb, s));
-  pl.splits = static_cast<int>(ceil_div(kb, pl.kb_per_split));
   const int act_rows = pl.swap ? pl.bn : kTile;
   const int w_rows = pl.swap ? kTile : pl.bn;
   const int stage_bytes = (act_rows + w_rows) * kKBytes;
-  // pipeline depth: small M takes just the CTA's k-blocks (a small footprint
-  // lets a dependent grid's CTAs be resident early and prefetch); large M
-  // and multi-tile walks take as many as fit
-  int want = kMaxStages;
-  if (pl.swap) {
-    const int per_cta = pl.splits > 1 ? pl.kb_per_split : kb;
-    want = per_cta < 2 ? 2 : (per_cta > kMaxStages ? kMaxStages : per_cta);
-    if (pl.splits == 1 && pl.num_tiles > sms) want = kMaxStages;
+
+  int s_max = 1;
+  if (pl.num_tiles < sms) {
+    s_max = sms / pl.num_tiles;
+    const int nchunks = pl.bn / pl.chunk_cols;
+    if (s_max > kMaxSplits) s_max = kMaxSplits;
+    if (s_max > nchunks) s_max = nchunks;
+    if (s_max > kb) s_max = kb;
+    if (s_max < 1) s_max = 1;
   }
-  // split-K receive buffers: a dedicated region (no barrier after the
-  // mainloop) or inside the stage buffers, whichever leaves the deeper
-  // pipeline (dedicated on a tie)
-  bool placed = false;
-  int best_st = 0;
-  bool best_in_stages = false;
-  for (int mode = 0; mode < (pl.splits > 1 ? 2 : 1); ++mode) {
-    pl.recv_in_stages = mode == 1;
-    for (int st = kMaxStages; st >= 2; --st) {
-      if (st > want && !(pl.recv_in_stages && st <= kMaxStages)) continue;
-      pl.stages = st;
-      if (layout(pl, stage_bytes)) {
-        // a receive region inside the stages may need more depth than wanted
-        const int eff = st > want ? want : st;
-        if (!placed || eff > best_st) {
-          placed = true;
-          best_st = eff;
-          best_in_stages = pl.recv_in_stages;
-        }
-        break;
-      }
+  for (int s = s_max; s >= 1; --s) {
+    pl.kb_per_split = static_cast<int>(ceil_div(kb, s));
+    pl.splits = static_cast<int>(ceil_div(kb, pl.kb_per_split));
+    // pipeline depth: small M takes just the CTA's k-blocks (a small
+    // footprint lets a dependent grid's CTAs be resident early and
+    // prefetch); large M and multi-tile walks take as many as fit
+    int want = kMaxStages;
+    if (pl.swap) {
+      const int per_cta = pl.splits > 1 ? pl.kb_per_split : kb;
+      want = per_cta < 2 ? 2 : (per_cta > kMaxStages ? kMaxStages : per_cta);
+      if (pl.splits == 1 && pl.num_tiles > sms) want = kMaxStages;
     }
-  }
-  if (placed) {
-    pl.recv_in_stages = best_in_stages;
-    for (int st = best_in_stages ? kMaxStages : want; st >= 2; --st) {
-      pl.stages = st;
-      if (layout(pl, stage_bytes)) break;
-    }
-  }
-  if (!placed) {  // no split fits: run unsplit
-    pl.splits = 1;
-    pl.kb_per_split = kb;
-    pl.recv_in_stages = false;
-    for (int st = kMaxStages; st >= 2 && !placed; --st) {
-      pl.stages = st;
-      placed = layout(pl, stage_bytes);
-    }
+    if (!place_buffers(pl, stage_bytes, want)) continue;
+    if (pl.splits == 1) break;
+    const int capacity = fp8 ? cluster_capacity_for<true>(pl.swap, pl.bn, pl.splits, pl.smem)
+                             : cluster_capacity_for<false>(pl.swap, pl.bn, pl.splits, pl.smem);
+    if (capacity >= pl.num_tiles) break;
   }
   if (pl.splits > 1)
     pl.grid = dim3(static_cast<unsigned>(pl.num_tiles), 1, static_cast<unsigned>(pl.splits));
@@ -714,19 +799,8 @@ template <bool kFp8, bool kSwap, int kBN>
 cudaError_t launch_one(const CUtensorMap& ta, const CUtensorMap& to, const GemmArgs& a,
                        const Plan& pl, cudaStream_t stream) {
   auto kern = gemm_tc_kernel<kFp8, kSwap, kBN>;
-  static std::mutex mu;
-  static bool attr_set[64] = {false};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  {
-    std::lock_guard<std::mutex> lock(mu);
-    if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-      cudaError_t e =
-          cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
-      if (e != cudaSuccess) return e;
-      attr_set[dev] = true;
-    }
-  }
+  cudaError_t e = prepare_kernel<kFp8, kSwap, kBN>();
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = pl.grid;
   cfg.blockDim = dim3(kThreads);
@@ -778,7 +852,7 @@ frt_status gemm_common(bool fp8, const void* a, int64_t lda, const float* a_scal
 
   auto encode = tensor_map_encoder();
   if (!encode) return FRT_ERR_CUDA;
-  const Plan pl = make_plan(M, N, K, esize);
+  const Plan pl = make_plan(M, N, K, esize, fp8);
 
   CUtensorMap ta, to;
   {
