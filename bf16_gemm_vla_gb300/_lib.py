@@ -7,6 +7,12 @@ LIB_PATH = os.path.join(HERE, "libfrt.so")
 
 # frt_status
 FRT_OK = 0
+FRT_ERR_INVALID_ARG = 1
+FRT_ERR_UNSUPPORTED_SHAPE = 2
+FRT_ERR_MISALIGNED = 3
+FRT_ERR_WORKSPACE_TOO_SMALL = 4
+FRT_ERR_CUDA = 5
+FRT_ERR_TIMEOUT = 6
 STATUS_NAMES = {
     0: "FRT_OK", 1: "FRT_ERR_INVALID_ARG", 2: "FRT_ERR_UNSUPPORTED_SHAPE",
     3: "FRT_ERR_MISALIGNED", 4: "FRT_ERR_WORKSPACE_TOO_SMALL", 5: "FRT_ERR_CUDA",
@@ -31,6 +37,8 @@ SIGNATURES = {
     "frt_quantize_workspace_bytes": (_c_sz, [_c_i64, _c_i64, _c_int]),
     "frt_quantize_e4m3": (_c_int, [_c_p, _c_int, _c_i64, _c_i64, _c_i64, _c_int, _c_int, _c_p,
                                    _c_p, _c_p, _c_p, _c_sz, _c_p]),
+    "frt_quantize_e4m3_noalloc": (_c_int, [_c_p, _c_int, _c_i64, _c_i64, _c_i64, _c_int, _c_int,
+                                           _c_p, _c_p, _c_p, _c_p]),
     "frt_fnuz_to_ocp": (_c_int, [_c_p, _c_p, _c_sz, _c_p]),
     "frt_packed_weight_bytes": (_c_sz, [_c_i64, _c_i64, _c_int]),
     "frt_pack_weights": (_c_int, [_c_p, _c_int, _c_i64, _c_i64, _c_i64, _c_int, _c_p, _c_sz,

@@ -7,6 +7,8 @@
 // DeepSeek-V4-Flash on AMD MI300X", "The FP8 dialect problem").
 #include <cuda_bf16.h>
 
+#include <mutex>
+
 #include "frt_device.cuh"
 #include "frt_host.h"
 
@@ -379,4 +381,87 @@ extern "C" frt_status frt_fnuz_to_ocp(const uint8_t* in, uint8_t* out, size_t n,
     fnuz_to_ocp_byte_kernel<<<grid, 256, 0, st>>>(in, out, n);
   }
   return launch_status();
+}
+
+// ------------------------------------------------------------------ quantize without allocation
+//
+// Some callers cannot allocate device memory: a real-time control loop that
+// forbids allocator calls once it is running, a plugin that only receives
+// raw device pointers from a host application, or code that records a CUDA
+// graph in a mode where allocation would break the capture.  For them,
+// frt_quantize_e4m3_noalloc keeps its scratch (the amax partials) in the
+// fixed array below instead of a caller-provided workspace.  Every GPU that
+// loads the library holds the array until the process exits.
+
+namespace frt {
+namespace {
+
+constexpr int64_t kNoAllocScratchFloats = 262144;  // 1 MiB
+
+static __device__ __align__(256) float g_noalloc_scratch[kNoAllocScratchFloats];
+
+// Device address of the scratch array on the current device.  In host code
+// the array's name is only a host-side stand-in, so the address is looked up
+// once per device (with that device current) and cached.
+float* noalloc_scratch(frt_status* status) {
+  static std::mutex mu;
+  static float* addr[64] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();
+    *status = FRT_ERR_CUDA;
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
+      cudaGetLastError();
+      *status = FRT_ERR_CUDA;
+      return nullptr;
+    }
+    addr[dev] = static_cast<float*>(p);
+  }
+  return addr[dev];
+}
+
+}  // namespace
+}  // namespace frt
+
+extern "C" frt_status frt_quantize_e4m3_noalloc(const void* x, frt_dtype x_dtype, int64_t rows,
+                                                int64_t cols, int64_t ldx, frt_scale_mode mode,
+                                                frt_dtype out_fmt, const float* static_scale,
+                                                uint8_t* q, float* scale, frt_stream_t stream) {
+  using namespace frt;
+  if (x_dtype != FRT_BF16 && x_dtype != FRT_F32) return FRT_ERR_INVALID_ARG;
+  if (out_fmt != FRT_E4M3_OCP && out_fmt != FRT_E4M3_FNUZ) return FRT_ERR_INVALID_ARG;
+  if (mode != FRT_SCALE_PER_TENSOR && mode != FRT_SCALE_PER_COL) return FRT_ERR_INVALID_ARG;
+  if (rows < 0 || cols < 0 || ldx < cols) return FRT_ERR_INVALID_ARG;
+  if (rows == 0 || cols == 0) return FRT_OK;
+  if (!x || !q) return FRT_ERR_INVALID_ARG;
+  if (rows > (1LL << 40) || cols > (1LL << 31)) return FRT_ERR_UNSUPPORTED_SHAPE;
+  const size_t esize = x_dtype == FRT_BF16 ? 2 : 4;
+  if (!aligned(x, esize) || (scale && !aligned(scale, 4)) ||
+      (static_scale && !aligned(static_scale, 4)))
+    return FRT_ERR_MISALIGNED;
+  // the scratch holds at most kNoAllocScratchFloats partial maxima
+  if (!static_scale && frt_quantize_workspace_bytes(rows, cols, mode) >
+                           static_cast<size_t>(kNoAllocScratchFloats) * sizeof(float))
+    return FRT_ERR_UNSUPPORTED_SHAPE;
+  frt_status st = FRT_OK;
+  float* ws = noalloc_scratch(&st);
+  if (!ws) return st;
+  cudaStream_t s = as_cuda(stream);
+  const bool fnuz = out_fmt == FRT_E4M3_FNUZ;
+  if (x_dtype == FRT_BF16) {
+    const auto* xb = static_cast<const __nv_bfloat16*>(x);
+    return fnuz ? quantize_typed<__nv_bfloat16, true>(xb, rows, cols, ldx, mode, static_scale, q,
+                                                      scale, ws, s)
+                : quantize_typed<__nv_bfloat16, false>(xb, rows, cols, ldx, mode, static_scale,
+                                                       q, scale, ws, s);
+  }
+  const auto* xf = static_cast<const float*>(x);
+  return fnuz ? quantize_typed<float, true>(xf, rows, cols, ldx, mode, static_scale, q, scale, ws, s)
+              : quantize_typed<float, false>(xf, rows, cols, ldx, mode, static_scale, q, scale,
+                                             ws, s);
 }

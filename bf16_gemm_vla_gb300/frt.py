@@ -78,6 +78,23 @@ def frt_quantize_e4m3(x, mode=PER_TENSOR, out_fmt=OCP, static_scale=None, q=None
     return q, scale
 
 
+def frt_quantize_e4m3_noalloc(x, mode=PER_TENSOR, out_fmt=OCP, static_scale=None, q=None,
+                              scale=None, stream=None):
+    """frt_quantize_e4m3 for callers that cannot allocate device memory: the
+    amax partials use a fixed 1 MiB array inside the library.  Pass q and
+    scale in to allocate nothing at all."""
+    rows, cols, ldx = _rows_view(x, "x")
+    if q is None:
+        q = torch.empty((rows, cols), dtype=torch.uint8, device=x.device)
+    if scale is None:
+        scale = torch.empty((cols if mode == PER_COL else 1,), dtype=torch.float32, device=x.device)
+    _check("frt_quantize_e4m3_noalloc",
+           lib().frt_quantize_e4m3_noalloc(x.data_ptr(), _XDT[x.dtype], rows, cols, ldx,
+                                           _MODE[mode], _FMT[out_fmt], _ptr(static_scale),
+                                           q.data_ptr(), _ptr(scale), _stream(stream)))
+    return q, scale
+
+
 # ---------------------------------------------------------------- FNUZ -> OCP
 
 def frt_fnuz_to_ocp(inp, out=None, stream=None):

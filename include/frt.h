@@ -119,6 +119,33 @@ frt_status frt_quantize_e4m3(const void* x, frt_dtype x_dtype, int64_t rows, int
                              void* workspace, size_t workspace_bytes, frt_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Quantization without allocation.  The source pages have no counterpart:
+ * this entry point exists for callers that cannot allocate device memory --
+ * a real-time control loop that forbids allocator calls once it runs, a
+ * plugin that only receives raw device pointers from its host application,
+ * or code recording a CUDA graph in a mode where allocating would break the
+ * capture.  It computes exactly what frt_quantize_e4m3 computes, with the
+ * same arguments minus the workspace: the amax partials live in a fixed
+ * 1 MiB array inside the library (262144 floats), which every GPU that loads
+ * the library keeps until the process exits.
+ *   - Nothing is allocated or freed, by this call or by any routine it calls.
+ *   - Size limit (only when static_scale is NULL): the workspace that
+ *     frt_quantize_workspace_bytes() reports must be at most 1 MiB -- always
+ *     true per tensor; per column ceil(rows / 64) * cols <= 262144.  Larger
+ *     shapes return FRT_ERR_UNSUPPORTED_SHAPE and enqueue nothing.
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current) and caches it; make that first call before any
+ *     stream capture.
+ *   - All calls share the one array, and each call overwrites the partials
+ *     it reads, so nothing needs clearing between calls; calls that overlap
+ *     on the GPU (different streams, no ordering) race on it.
+ * ---------------------------------------------------------------------- */
+frt_status frt_quantize_e4m3_noalloc(const void* x, frt_dtype x_dtype, int64_t rows, int64_t cols,
+                                     int64_t ldx, frt_scale_mode mode, frt_dtype out_fmt,
+                                     const float* static_scale, uint8_t* q, float* scale,
+                                     frt_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * FNUZ -> OCP re-encoding of n E4M3 bytes ("Real-time VLA inference on AMD
  * hardware", "Different FP8 representation").  Each output byte is the OCP
  * code of the FNUZ byte's value: exponent field e >= 2 keeps sign and
