@@ -109,6 +109,37 @@ def aggregate(units_per_rank, seconds_per_rank, world, device=None):
 
 # ---------------------------------------------------------------- peaks and clocks
 
+def gemm_source_hash():
+    import hashlib
+
+    h = hashlib.sha256()
+    for f in ("bf16_gemm_vla_gb300/csrc/frt_gemm.cu", "bf16_gemm_vla_gb300/csrc/frt_device.cuh"):
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(shapes):
+    """Mean DRAM bytes per launch over `shapes` [(M, K, N)] from the committed ncu
+    figures, or None when the GEMM sources changed since they were taken."""
+    path = os.path.join(ROOT, "profiles", "gemm_fp8_dram_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    src, table = None, {}
+    with open(path) as f:
+        for line in f:
+            parts = line.split()
+            if not parts or parts[0].startswith("#"):
+                continue
+            if parts[0] == "source":
+                src = parts[1]
+            elif len(parts) == 4:
+                table[tuple(int(x) for x in parts[:3])] = float(parts[3])
+    if src != gemm_source_hash() or not all(tuple(s) in table for s in shapes):
+        return None
+    return sum(table[tuple(s)] for s in shapes) / len(shapes)
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -325,8 +356,10 @@ def run_headline(args, device, world, sampler, peaks, peak_kind):
                            "gemm_tflops": f / g / 1e12, "quantize_us": q * 1e6})
     fp8_peak = peaks["bf16_tflops_sustained"] * FP8_OVER_BF16
     achieved = tot_flops / tot_time / 1e12
+    traffic = profiled_traffic([(M_ENC, lin.w.K, lin.w.N) for lin in set0.layers])
     roofline = {"bound": "tensor", "achieved": achieved, "peak": fp8_peak, "unit": "TFLOP/s",
-                "frac": achieved / fp8_peak, "traffic": None,
+                "frac": achieved / fp8_peak, "traffic": traffic,
+                "traffic_unit": "bytes per launch (mean over the step's 3 GEMM launches, ncu)",
                 "kernel": "gemm_tc_kernel<fp8, 128x256 tiles>",
                 "peak_source": "%s bf16 sustained x %.0f (nominal FP8/BF16 dense ratio), of %s"
                                % (peak_kind, FP8_OVER_BF16, peak_kind),
