@@ -101,6 +101,84 @@ __device__ __forceinline__ uint32_t encode_e4m3(float v) {
   return sign | mag;
 }
 
+// OCP E4M3 byte of a value by the hardware conversion (round to nearest
+// even, saturating to +-448).  Used only for finite values in the E4M3
+// normal range, where it agrees with encode_e4m3<false>.
+__device__ __forceinline__ uint32_t cvt_e4m3_ocp(float v) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(0.0f), "f"(v));
+  return r & 0xFFu;
+}
+
+// E4M3 byte of the IEEE fp32 quotient x / s.
+//
+// Fast path: q = x * r with r = RN(1/s).  q and RN(x/s) both lie within a
+// relative 2^-23 of x / s (two and one roundings of at most 2^-24), so they
+// are at most 6 fp32 steps apart (a step halves just below a power of two).
+// E4M3 rounding is monotone and only changes at midpoints between codes,
+// which in the E4M3 normal range are the fp32 values whose low 20 mantissa
+// bits are 0x80000.  When q is finite, in the normal range, and at least 9
+// steps from such a midpoint, q and RN(x/s) therefore encode to the same
+// byte and q is encoded.  Every other element takes the IEEE division.
+// `fast_ok` (uniform) says r is a positive normal number.
+template <bool kFnuz>
+__device__ __forceinline__ uint32_t quantize_one(float x, float s, float r, bool fast_ok) {
+  constexpr uint32_t kMinNormalBits = kFnuz ? 0x3C000000u : 0x3C800000u;  // 2^-7 / 2^-6
+  if (fast_ok) {
+    const float q = x * r;
+    const uint32_t u = __float_as_uint(q) & 0x7FFFFFFFu;
+    const uint32_t m = u & 0xFFFFFu;
+    const uint32_t d = m >= 0x80000u ? m - 0x80000u : 0x80000u - m;
+    if (u >= kMinNormalBits && u < 0x7F800000u && d > 8u) {
+      if constexpr (kFnuz)
+        return encode_e4m3<true>(q);
+      else
+        return cvt_e4m3_ocp(q);
+    }
+  }
+  return encode_e4m3<kFnuz>(__fdiv_rn(x, s));
+}
+
+// OCP E4M3 bytes of the IEEE fp32 quotients a / s and b / s (a in the low
+// byte).  Fast path: with y = v * r (r = RN(1/s)), RN(v / s) lies within a
+// relative 1.5 * 2^-23 of y, so inside [y (1 - 2^-20), y (1 + 2^-20)] even
+// after the bracket's own rounding.  E4M3 rounding is monotone, so when
+// both ends of the bracket encode to the same byte, so does RN(v / s).  Two
+// hardware conversions give the ends of both elements' brackets; elements
+// whose bracket straddles a rounding midpoint take the IEEE division.
+__device__ __forceinline__ uint32_t cvt_e4m3x2_ocp(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t quantize_pair_ocp(float a, float b, float s, float r,
+                                                      bool fast_ok) {
+  if (fast_ok) {
+    const float ya = a * r, yb = b * r;
+    const float kDown = 1.0f - 0x1p-20f, kUp = 1.0f + 0x1p-20f;
+    const uint32_t c0 = cvt_e4m3x2_ocp(ya * kDown, yb * kDown);
+    const uint32_t c1 = cvt_e4m3x2_ocp(ya * kUp, yb * kUp);
+    if (c0 == c1) return c0;
+    uint32_t out = 0;
+    out |= ((c0 ^ c1) & 0x00FFu) ? encode_e4m3<false>(__fdiv_rn(a, s)) : (c0 & 0x00FFu);
+    out |= ((c0 ^ c1) & 0xFF00u) ? encode_e4m3<false>(__fdiv_rn(b, s)) << 8 : (c0 & 0xFF00u);
+    return out;
+  }
+  return encode_e4m3<false>(__fdiv_rn(a, s)) | (encode_e4m3<false>(__fdiv_rn(b, s)) << 8);
+}
+
+// NaN bytes (S.1111.111) of four OCP codes -> the positive NaN 0x7f.
+__device__ __forceinline__ uint32_t canonical_nan_x4(uint32_t w) {
+  const uint32_t t = (w & 0x7F7F7F7Fu) + 0x01010101u;  // bit 7 set where low 7 bits are 0x7f
+  return w & ~(t & 0x80808080u);
+}
+
+__device__ __forceinline__ bool recip_is_normal(float s, float r) {
+  const uint32_t e = __float_as_uint(r) >> 23;  // r > 0: the exponent field
+  return s > 0.0f && e - 1u < 254u;
+}
+
 // ------------------------------------------------------------------ quantize
 
 constexpr int kQThreads = 256;
@@ -151,36 +229,56 @@ __device__ __forceinline__ float block_max(float v, float* red) {
 }
 
 // Per-tensor pass 1: each block's max |x| (NaN ignored by fmaxf) -> partial[block].
-// Vector path: VEC = 8 elements per step; scalar path: VEC = 1.
+// Vector path: VEC = 8 elements per load, kUnroll loads in flight per
+// thread; scalar path: VEC = 1.
+constexpr int kUnroll = 4;
+
 template <typename T, int VEC>
 __global__ void __launch_bounds__(kQThreads) amax_tensor_kernel(const T* __restrict__ x,
                                                                int64_t rows, int64_t cols,
                                                                int64_t ldx,
                                                                float* __restrict__ partial) {
   __shared__ float red[32];
+  dev::grid_dependency_wait();  // x may come from the previous grid
   float m = 0.0f;
   const int64_t vpr = cols / VEC;  // vectors per row
   const int64_t total = rows * vpr;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   const bool dense = ldx == cols;
-  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
-       i += stride) {
-    int64_t off = i * VEC;
-    if (!dense) {
-      const int64_t r = i / vpr;
-      off = r * ldx + (i - r * vpr) * VEC;
-    }
+  auto offset = [&](int64_t i) -> int64_t {
+    if (dense) return i * VEC;
+    const int64_t r = i / vpr;
+    return r * ldx + (i - r * vpr) * VEC;
+  };
+  for (int64_t i0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i0 < total;
+       i0 += kUnroll * stride) {
     if constexpr (VEC == 8) {
-      float f[8];
-      load8<T>(x + off, f);
+      float f[kUnroll][8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) m = fmaxf(m, fabsf(f[e]));
+      for (int u = 0; u < kUnroll; ++u) {
+        const int64_t i = i0 + u * stride;
+        if (i < total) {
+          load8<T>(x + offset(i), f[u]);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) f[u][e] = 0.0f;
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) m = fmaxf(m, fabsf(f[u][e]));
     } else {
-      m = fmaxf(m, fabsf(to_f32<T>(x[off])));
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const int64_t i = i0 + u * stride;
+        if (i < total) m = fmaxf(m, fabsf(to_f32<T>(x[offset(i)])));
+      }
     }
   }
   m = block_max(m, red);
   if (threadIdx.x == 0) partial[blockIdx.x] = m;
+  dev::grid_launch_dependents();  // the encode pass may start once every block is here
 }
 
 // Per-tensor pass 2: reduce the partials to amax, s = amax / max (1 if amax
@@ -192,8 +290,13 @@ __global__ void __launch_bounds__(kQThreads) encode_tensor_kernel(
     uint8_t* __restrict__ q, float* __restrict__ scale_out) {
   __shared__ float red[32];
   __shared__ float s_sh;
-  // a GEMM launched after this grid may start fetching its weights now
-  dev::grid_launch_dependents();
+  dev::grid_dependency_wait();  // the partials and x come from earlier grids
+  const int64_t n_vec = rows * (cols / VEC);
+  const int64_t n_threads = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  // a short pass lets the next grid (typically a GEMM fetching its weights)
+  // start now; a long one triggers at its end so it does not compete
+  const bool early = n_vec <= 2 * kUnroll * n_threads;
+  if (early) dev::grid_launch_dependents();
   if (static_scale) {
     if (threadIdx.x == 0) s_sh = __ldg(static_scale);
   } else {
@@ -204,32 +307,59 @@ __global__ void __launch_bounds__(kQThreads) encode_tensor_kernel(
   }
   __syncthreads();
   const float s = s_sh;
+  const float r = __frcp_rn(s);
+  const bool fast_ok = recip_is_normal(s, r);
   if (blockIdx.x == 0 && threadIdx.x == 0 && scale_out) *scale_out = s;
   const int64_t vpr = cols / VEC;
   const int64_t total = rows * vpr;
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  const int64_t stride = n_threads;
   const bool dense = ldx == cols;
-  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
-       i += stride) {
-    int64_t off = i * VEC;  // q is dense: element (r, c) at r * cols + c = i * VEC
-    int64_t xoff = off;
-    if (!dense) {
-      const int64_t r = i / vpr;
-      xoff = r * ldx + (i - r * vpr) * VEC;
-    }
+  auto xoffset = [&](int64_t i) -> int64_t {
+    if (dense) return i * VEC;
+    const int64_t r = i / vpr;
+    return r * ldx + (i - r * vpr) * VEC;
+  };
+  for (int64_t i0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i0 < total;
+       i0 += kUnroll * stride) {
     if constexpr (VEC == 8) {
-      float f[8];
-      load8<T>(x + xoff, f);
-      uint32_t lo = 0, hi = 0;
+      float f[kUnroll][8];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) lo |= encode_e4m3<kFnuz>(__fdiv_rn(f[e], s)) << (8 * e);
+      for (int u = 0; u < kUnroll; ++u) {
+        const int64_t i = i0 + u * stride;
+        if (i < total) load8<T>(x + xoffset(i), f[u]);
+      }
 #pragma unroll
-      for (int e = 0; e < 4; ++e) hi |= encode_e4m3<kFnuz>(__fdiv_rn(f[4 + e], s)) << (8 * e);
-      *reinterpret_cast<uint2*>(q + off) = make_uint2(lo, hi);
+      for (int u = 0; u < kUnroll; ++u) {
+        const int64_t i = i0 + u * stride;
+        if (i >= total) break;
+        uint32_t lo = 0, hi = 0;
+        if constexpr (kFnuz) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) lo |= quantize_one<true>(f[u][e], s, r, fast_ok) << (8 * e);
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            hi |= quantize_one<true>(f[u][4 + e], s, r, fast_ok) << (8 * e);
+        } else {
+          lo = quantize_pair_ocp(f[u][0], f[u][1], s, r, fast_ok) |
+               (quantize_pair_ocp(f[u][2], f[u][3], s, r, fast_ok) << 16);
+          hi = quantize_pair_ocp(f[u][4], f[u][5], s, r, fast_ok) |
+               (quantize_pair_ocp(f[u][6], f[u][7], s, r, fast_ok) << 16);
+          lo = canonical_nan_x4(lo);
+          hi = canonical_nan_x4(hi);
+        }
+        // q is dense: element (r, c) at r * cols + c = i * VEC
+        *reinterpret_cast<uint2*>(q + i * VEC) = make_uint2(lo, hi);
+      }
     } else {
-      q[off] = static_cast<uint8_t>(encode_e4m3<kFnuz>(__fdiv_rn(to_f32<T>(x[xoff]), s)));
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const int64_t i = i0 + u * stride;
+        if (i < total)
+          q[i] = static_cast<uint8_t>(quantize_one<kFnuz>(to_f32<T>(x[xoffset(i)]), s, r, fast_ok));
+      }
     }
   }
+  if (!early) dev::grid_launch_dependents();
 }
 
 // Per-column pass 1: block (bx, by) covers columns [bx*256, +256) and rows
@@ -239,6 +369,7 @@ __global__ void __launch_bounds__(kQThreads) amax_col_kernel(const T* __restrict
                                                             int64_t rows, int64_t cols,
                                                             int64_t ldx,
                                                             float* __restrict__ partial) {
+  dev::grid_dependency_wait();
   const int64_t c = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (c >= cols) return;
   const int64_t r0 = static_cast<int64_t>(blockIdx.y) * kColRowsPerBlock;
@@ -255,6 +386,7 @@ __global__ void __launch_bounds__(kQThreads) encode_col_kernel(
     const T* __restrict__ x, int64_t rows, int64_t cols, int64_t ldx,
     const float* __restrict__ partial, int npartial, const float* __restrict__ static_scale,
     uint8_t* __restrict__ q, float* __restrict__ scale_out) {
+  dev::grid_dependency_wait();
   dev::grid_launch_dependents();
   const int64_t c = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (c >= cols) return;
@@ -267,17 +399,22 @@ __global__ void __launch_bounds__(kQThreads) encode_col_kernel(
     s = m == 0.0f ? 1.0f : __fdiv_rn(m, kFnuz ? 240.0f : 448.0f);
   }
   if (blockIdx.y == 0 && scale_out) scale_out[c] = s;
+  const float rs = __frcp_rn(s);
+  const bool fast_ok = recip_is_normal(s, rs);
   const int64_t r0 = static_cast<int64_t>(blockIdx.y) * kColRowsPerBlock;
   const int64_t r1 = min(rows, r0 + kColRowsPerBlock);
   for (int64_t r = r0; r < r1; ++r)
-    q[r * cols + c] = static_cast<uint8_t>(encode_e4m3<kFnuz>(__fdiv_rn(to_f32<T>(x[r * ldx + c]), s)));
+    q[r * cols + c] =
+        static_cast<uint8_t>(quantize_one<kFnuz>(to_f32<T>(x[r * ldx + c]), s, rs, fast_ok));
 }
 
-int tensor_grid(int64_t total_vecs) {
-  const int64_t want = ceil_div(total_vecs, kQThreads);
-  const int64_t cap = static_cast<int64_t>(sm_count() > 0 ? sm_count() : 148) * 4;
+// Blocks for a grid-stride pass over total_vecs vectors, kUnroll per thread
+// per iteration: at most `per_sm` blocks per SM and `limit` in total.
+int tensor_grid(int64_t total_vecs, int per_sm, int limit) {
+  const int64_t want = ceil_div(total_vecs, static_cast<int64_t>(kQThreads) * kUnroll);
+  const int64_t cap = static_cast<int64_t>(sm_count() > 0 ? sm_count() : 148) * per_sm;
   int64_t g = want < cap ? want : cap;
-  if (g > kMaxPartials) g = kMaxPartials;
+  if (g > limit) g = limit;
   return static_cast<int>(g < 1 ? 1 : g);
 }
 
@@ -288,15 +425,39 @@ frt_status quantize_typed(const T* x, int64_t rows, int64_t cols, int64_t ldx, f
   if (mode == FRT_SCALE_PER_TENSOR) {
     const bool vec = aligned(x, 16) && aligned(q, 8) && cols % 8 == 0 && ldx % 8 == 0;
     const int64_t total = rows * (vec ? cols / 8 : cols);
-    const int grid = tensor_grid(total);
+    const int grid = tensor_grid(total, 6, kMaxPartials);  // amax: one partial per block
+    const int egrid = tensor_grid(total, 8, 1 << 20);
+    // programmatic launches: each kernel's blocks may be scheduled while the
+    // previous grid drains, and wait for it before reading its output
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cudaLaunchConfig_t ecfg;
+    cfg.blockDim = dim3(kQThreads);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    ecfg = cfg;
+    ecfg.gridDim = dim3(egrid);
+    cudaError_t e = cudaSuccess;
     if (vec) {
-      if (!static_scale) amax_tensor_kernel<T, 8><<<grid, kQThreads, 0, st>>>(x, rows, cols, ldx, ws);
-      encode_tensor_kernel<T, 8, kFnuz>
-          <<<grid, kQThreads, 0, st>>>(x, rows, cols, ldx, ws, grid, static_scale, q, scale);
+      if (!static_scale)
+        e = cudaLaunchKernelEx(&cfg, amax_tensor_kernel<T, 8>, x, rows, cols, ldx, ws);
+      if (e == cudaSuccess)
+        e = cudaLaunchKernelEx(&ecfg, encode_tensor_kernel<T, 8, kFnuz>, x, rows, cols, ldx,
+                               static_cast<const float*>(ws), grid, static_scale, q, scale);
     } else {
-      if (!static_scale) amax_tensor_kernel<T, 1><<<grid, kQThreads, 0, st>>>(x, rows, cols, ldx, ws);
-      encode_tensor_kernel<T, 1, kFnuz>
-          <<<grid, kQThreads, 0, st>>>(x, rows, cols, ldx, ws, grid, static_scale, q, scale);
+      if (!static_scale)
+        e = cudaLaunchKernelEx(&cfg, amax_tensor_kernel<T, 1>, x, rows, cols, ldx, ws);
+      if (e == cudaSuccess)
+        e = cudaLaunchKernelEx(&ecfg, encode_tensor_kernel<T, 1, kFnuz>, x, rows, cols, ldx,
+                               static_cast<const float*>(ws), grid, static_scale, q, scale);
+    }
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return FRT_ERR_CUDA;
     }
   } else {
     const dim3 grid(static_cast<unsigned>(ceil_div(cols, kQThreads)),

@@ -90,10 +90,10 @@ struct Cfg {
   static constexpr int kActBytes = kActRows * kKBytes;
   static constexpr int kWBytes = kWRows * kKBytes;
   static constexpr int kStageBytes = kActBytes + kWBytes;
-  static constexpr int kTmemCols = kSwap ? 2 * kBN : 512;  // two accumulator buffers
+  static constexpr int kTmemCols = 2 * kBN;  // two accumulator buffers
   static_assert(kActBytes % 1024 == 0 && kWBytes % 1024 == 0, "operand tiles 1024-aligned");
   static_assert(kBN == 32 || kBN == 64 || kBN == 128 || kBN == 256, "tile width");
-  static_assert(kSwap || kBN == 256, "large-M tiles are 128 x 256");
+  static_assert(kSwap || kBN >= 128, "large-M tiles are 128 x 128 or 128 x 256");
 };
 
 // tanh-GELU, 0.5 v (1 + tanh(u)) with u = sqrt(2/pi) (v + 0.044715 v^3),
@@ -697,7 +697,9 @@ int cluster_capacity(int s, int smem) {
 
 template <bool kFp8>
 int cluster_capacity_for(bool swap, int bn, int s, int smem) {
-  if (!swap) return cluster_capacity<kFp8, false, 256>(s, smem);
+  if (!swap)
+    return bn == 128 ? cluster_capacity<kFp8, false, 128>(s, smem)
+                     : cluster_capacity<kFp8, false, 256>(s, smem);
   switch (bn) {
     case 32: return cluster_capacity<kFp8, true, 32>(s, smem);
     case 64: return cluster_capacity<kFp8, true, 64>(s, smem);
@@ -749,10 +751,16 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int esize, bool fp8) {
     pl.tiles_m = static_cast<int>(ceil_div(M, pl.bn));
     pl.chunk_cols = 8;
   } else {
+    // 128 x 256 tiles carry the most FLOPs per byte a CTA ingests; when they
+    // would leave most SMs idle on a short K loop, 128 x 128 tiles fill the
+    // machine without a split-K exchange
     pl.swap = false;
-    pl.bn = 256;
     pl.tiles_m = static_cast<int>(ceil_div(M, kTile));
-    pl.tiles_n = static_cast<int>(ceil_div(N, 256));
+    const int sms0 = sm_count() > 0 ? sm_count() : 148;
+    const int64_t wide = pl.tiles_m * ceil_div(N, 256);
+    const int64_t narrow = pl.tiles_m * ceil_div(N, 128);
+    pl.bn = (2 * wide <= sms0 && narrow <= sms0 && kb <= 32) ? 128 : 256;
+    pl.tiles_n = static_cast<int>(ceil_div(N, pl.bn));
     pl.chunk_cols = 32;
   }
   pl.num_tiles = pl.tiles_m * pl.tiles_n;
@@ -821,7 +829,9 @@ cudaError_t launch_one(const CUtensorMap& ta, const CUtensorMap& to, const GemmA
 template <bool kFp8>
 cudaError_t dispatch(const CUtensorMap& ta, const CUtensorMap& to, const GemmArgs& a,
                      const Plan& pl, cudaStream_t stream) {
-  if (!pl.swap) return launch_one<kFp8, false, 256>(ta, to, a, pl, stream);
+  if (!pl.swap)
+    return pl.bn == 128 ? launch_one<kFp8, false, 128>(ta, to, a, pl, stream)
+                        : launch_one<kFp8, false, 256>(ta, to, a, pl, stream);
   switch (pl.bn) {
     case 32: return launch_one<kFp8, true, 32>(ta, to, a, pl, stream);
     case 64: return launch_one<kFp8, true, 64>(ta, to, a, pl, stream);

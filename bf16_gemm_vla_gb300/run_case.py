@@ -1,6 +1,7 @@
 """Runs one layer of the path a few times, for profiling (e.g. under ncu).
 
     python -m bf16_gemm_vla_gb300.run_case --kind fp8 --M 50 --K 1024 --N 4096 --reps 3
+    python -m bf16_gemm_vla_gb300.run_case --op quantize --M 768 --K 16384 --reps 3
 
 Synthetic inputs are drawn on the device (seeded): activations N(0,1) bf16,
 weights N(0,0.02), bias N(0,0.1).  The FP8 path quantizes the activations
@@ -26,8 +27,12 @@ def main(argv=None):
     ap.add_argument("--reps", type=int, default=3)
     ap.add_argument("--with-quantize", action="store_true")
     ap.add_argument("--quiet", action="store_true")
+    ap.add_argument("--op", choices=("gemm", "quantize"), default="gemm")
+    ap.add_argument("--static-scale", action="store_true")
     a = ap.parse_args(argv)
     dev = torch.device("cuda")
+    if a.op == "quantize":
+        return quantize_case(a, dev)
     g = torch.Generator(device=dev)
     g.manual_seed(0)
     x = torch.randn((a.M, a.K), generator=g, device=dev).to(torch.bfloat16)
@@ -60,6 +65,32 @@ def main(argv=None):
     if not a.quiet:
         print("%s M=%d K=%d N=%d: %.2f us per launch" % (a.kind, a.M, a.K, a.N,
                                                           e0.elapsed_time(e1) * 1e3 / a.reps))
+
+
+def quantize_case(a, dev):
+    g = torch.Generator(device=dev)
+    g.manual_seed(0)
+    x = torch.randn((a.M, a.K), generator=g, device=dev).to(torch.bfloat16)
+    q = torch.empty((a.M, a.K), dtype=torch.uint8, device=dev)
+    s = torch.empty((1,), dtype=torch.float32, device=dev)
+    ws = torch.empty((4096,), dtype=torch.float32, device=dev)
+    one = torch.ones((1,), dtype=torch.float32, device=dev)
+
+    def once():
+        frt.frt_quantize_e4m3(x, static_scale=one if a.static_scale else None, q=q, scale=s,
+                              workspace=ws)
+
+    once()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(a.reps):
+        once()
+    e1.record()
+    torch.cuda.synchronize()
+    if not a.quiet:
+        print("quantize %d x %d: %.2f us per call" % (a.M, a.K, e0.elapsed_time(e1) * 1e3 / a.reps))
 
 
 if __name__ == "__main__":

@@ -180,3 +180,33 @@ def test_quantize_student_t_full_size():
     qh = q.view(-1).cpu().numpy()
     ref = e4m3.encode(quantize.divide_f32(xh[idx], so), e4m3.OCP)
     np.testing.assert_array_equal(qh[idx], ref)
+
+
+@pytest.mark.parametrize("fmt,ofmt", FMTS)
+def test_quotients_near_rounding_midpoints(fmt, ofmt):
+    # x is built so that x / s lands within +-12 fp32 steps of every midpoint
+    # between adjacent E4M3 codes, for many scales: the region where a
+    # quotient computed by a reciprocal could round differently from the
+    # IEEE quotient.  Bytes must equal the oracle's (IEEE fp32 division).
+    t = e4m3.decode_table(ofmt)
+    pos = np.unique(t[(t > 0) & ~np.isnan(t)])
+    mids = np.float32((pos[1:] + pos[:-1]) / 2)
+    steps = np.arange(-12, 13, dtype=np.int64)
+    g = np.random.default_rng(17)
+    for s in np.float32(np.concatenate([g.uniform(1e-3, 4.0, 6), [1.0, 0.5, 3.0 / 448]])):
+        target = (mids.view(np.int32)[:, None] + steps[None, :]).astype(np.int32).view(np.float32)
+        x = np.float32(target.astype(np.float64) * np.float64(s)).reshape(-1)
+        x = np.concatenate([x, -x])
+        x = np.concatenate([x, np.zeros((-len(x)) % 8, dtype=np.float32)]).reshape(-1, 8)
+        sd = torch.tensor([s], dtype=torch.float32, device="cuda")
+        for dt in (torch.float32,):
+            q, _ = frt.frt_quantize_e4m3(torch.from_numpy(x).cuda().to(dt), frt.PER_TENSOR, fmt,
+                                         static_scale=sd)
+            qo, _ = quantize.quantize_e4m3(x, quantize.PER_TENSOR, ofmt, static_scale=s)
+            np.testing.assert_array_equal(q.cpu().numpy(), qo)
+        # the same values as one column of a per-column quantize
+        xc = np.ascontiguousarray(x.reshape(-1, 1))
+        q, _ = frt.frt_quantize_e4m3(torch.from_numpy(xc).cuda(), frt.PER_COL, fmt,
+                                     static_scale=torch.tensor([s], device="cuda"))
+        qo, _ = quantize.quantize_e4m3(xc, quantize.PER_COL, ofmt, static_scale=np.float32([s]))
+        np.testing.assert_array_equal(q.cpu().numpy(), qo)
