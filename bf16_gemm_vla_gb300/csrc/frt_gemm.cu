@@ -228,7 +228,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // thread arrives now (its mbarriers are initialised); when the receive
   // buffers reuse the stage buffers, each thread arrives once this CTA's
   // MMAs can no longer read them.
-  if (split && !p.recv_in_stages) dev::cluster_arrive();
+  if (split && !p.recv_in_stages) dev::cluster_arrive_relaxed();
 
   // this CTA's tiles: split -> one tile and a K range; else a strided list
   const int kb0 = split ? rank * p.kb_per_split : 0;
@@ -460,77 +460,158 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int owned = own_c1 - own_c0;
         if (p.recv_in_stages) dev::cluster_arrive();  // this CTA's stage buffers are free
         // 1. the chunks other ranks own -> this CTA's send buffer (stage region)
-        for (int c = 0; c < NC; ++c) {
-          if (c >= own_c0 && c < own_c1) continue;
-          const int sp = c < own_c0 ? c : c - owned;  // position in the send buffer
-          uint8_t* dst = base + sp * chunk_bytes;
-          if (CW == 32) {
+        if constexpr (kSwap) {
+          // 8-column chunks, read from TMEM up to 64 columns (one wait) at a time
+          constexpr int kPiece = kBN < 64 ? kBN : 64;
+#pragma unroll 1
+          for (int c64 = 0; c64 < kBN; c64 += kPiece) {
+            const int cb = c64 / 8;
+            if (cb >= own_c0 && cb + kPiece / 8 <= own_c1) continue;  // all owned
+            float v[kPiece];
+            if constexpr (kPiece == 64)
+              dev::tmem_ld64(tacc + c64, v);
+            else
+              dev::tmem_ld32(tacc + c64, v);
+#pragma unroll
+            for (int j = 0; j < kPiece / 8; ++j) {
+              const int c = cb + j;
+              if (c >= own_c0 && c < own_c1) continue;
+              uint8_t* dst = base + (c < own_c0 ? c : c - owned) * chunk_bytes;
+              *reinterpret_cast<float4*>(dst + chunk_off(row, 0, 8)) =
+                  make_float4(v[8 * j], v[8 * j + 1], v[8 * j + 2], v[8 * j + 3]);
+              *reinterpret_cast<float4*>(dst + chunk_off(row, 1, 8)) =
+                  make_float4(v[8 * j + 4], v[8 * j + 5], v[8 * j + 6], v[8 * j + 7]);
+            }
+          }
+        } else {
+          for (int c = 0; c < NC; ++c) {
+            if (c >= own_c0 && c < own_c1) continue;
+            uint8_t* dst = base + (c < own_c0 ? c : c - owned) * chunk_bytes;
             float v[32];
             dev::tmem_ld32(tacc + c * 32, v);
 #pragma unroll
             for (int q = 0; q < 8; ++q)
               *reinterpret_cast<float4*>(dst + chunk_off(row, q, 32)) =
                   make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-          } else {
-            float v[8];
-            dev::tmem_ld8(tacc + c * 8, v);
-            *reinterpret_cast<float4*>(dst + chunk_off(row, 0, 8)) =
-                make_float4(v[0], v[1], v[2], v[3]);
-            *reinterpret_cast<float4*>(dst + chunk_off(row, 1, 8)) =
-                make_float4(v[4], v[5], v[6], v[7]);
           }
         }
         dev::fence_proxy_async_smem();
-        dev::named_sync(1, 128);
-        // 2. after phase 1 (every peer initialised and its receive buffer
-        //    free), one bulk copy per owner
-        dev::cluster_wait();
-        if (et == 0) {
-          for (int o = 0; o < S; ++o) {
-            if (o == rank) continue;
+        if constexpr (kSwap) {
+          // 2. after phase 1 (every peer initialised), each warp copies its
+          //    own 32 rows of every chunk to the chunk's owner
+          __syncwarp();
+          dev::cluster_wait();
+          if (lane < S && lane != rank) {
+            const int o = lane;
             const int oc0 = chunk_begin(o), oc1 = chunk_begin(o + 1);
-            const int sp0 = oc0 < own_c0 ? oc0 : oc0 - owned;
             const int slot = rank < o ? rank : rank - 1;
-            const uint32_t dst = dev::map_to_rank(
-                sbase + p.recv_off + static_cast<uint32_t>(slot * owned_max) * chunk_bytes, o);
-            dev::bulk_copy_to_peer(dst, sbase + sp0 * chunk_bytes,
-                                   static_cast<uint32_t>(oc1 - oc0) * chunk_bytes,
-                                   dev::map_to_rank(recv_bar, o));
+            const uint32_t bar = dev::map_to_rank(recv_bar, o);
+            for (int c = oc0; c < oc1; ++c) {
+              const int sp = c < own_c0 ? c : c - owned;
+              const uint32_t rows_off = static_cast<uint32_t>(ew * 32 * CW * 4);
+              const uint32_t dst = dev::map_to_rank(
+                  sbase + p.recv_off +
+                      static_cast<uint32_t>(slot * owned_max + (c - oc0)) * chunk_bytes + rows_off,
+                  o);
+              dev::bulk_copy_to_peer(dst, sbase + sp * chunk_bytes + rows_off,
+                                     static_cast<uint32_t>(32 * CW * 4), bar);
+            }
+          }
+        } else {
+          dev::named_sync(1, 128);
+          // 2. after phase 1 (every peer initialised and its receive buffer
+          //    free), one bulk copy per owner
+          dev::cluster_wait();
+          if (et == 0) {
+            for (int o = 0; o < S; ++o) {
+              if (o == rank) continue;
+              const int oc0 = chunk_begin(o), oc1 = chunk_begin(o + 1);
+              const int sp0 = oc0 < own_c0 ? oc0 : oc0 - owned;
+              const int slot = rank < o ? rank : rank - 1;
+              const uint32_t dst = dev::map_to_rank(
+                  sbase + p.recv_off + static_cast<uint32_t>(slot * owned_max) * chunk_bytes, o);
+              dev::bulk_copy_to_peer(dst, sbase + sp0 * chunk_bytes,
+                                     static_cast<uint32_t>(oc1 - oc0) * chunk_bytes,
+                                     dev::map_to_rank(recv_bar, o));
+            }
           }
         }
         // 3. own chunks: own partial + received partials, in rank order
         ok = dev::mbar_wait(recv_bar, 0, abort_flag, p.dev_status, dev::kTimeoutEpilogue) && ok;
         ok = __all_sync(0xffffffffu, ok);
-        dev::cluster_arrive();  // phase 2: every copy into this CTA has landed
+        dev::cluster_arrive_relaxed();  // phase 2: every copy into this CTA has landed
         const uint8_t* recv = base + p.recv_off;
-        for (int c = own_c0; c < own_c1; ++c) {
-          const int lc = c - own_c0;
-          float acc[32];
-          if (CW == 32) {
-            dev::tmem_ld32(tacc + c * 32, acc);
-          } else {
-            float w8[8];
-            dev::tmem_ld8(tacc + c * 8, w8);
+        if constexpr (kSwap) {
+          // all owned rows of this warp are staged first (rows lc*8.. of the
+          // warp's two 32-row buffers), then one fence and one store per chunk
+#pragma unroll 1
+          for (int lc = 0; lc < owned; ++lc) {
+            float own[8];
+            dev::tmem_ld8(tacc + (own_c0 + lc) * 8, own);
+            // the S partials in rank order, this CTA's own at its rank; the
+            // receive slots hold the other ranks in rank order
+            float sum[8];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) acc[j] = w8[j];
+            for (int j = 0; j < 8; ++j) sum[j] = 0.0f;
 #pragma unroll
-            for (int j = 8; j < 32; ++j) acc[j] = 0.0f;
+            for (int r = 0; r < kMaxSplits; ++r) {
+              if (r >= S) break;
+              if (r == rank) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) sum[j] += own[j];
+              } else {
+                const uint8_t* src =
+                    recv + ((r < rank ? r : r - 1) * owned_max + lc) * chunk_bytes;
+                const float4 x0 = *reinterpret_cast<const float4*>(src + chunk_off(row, 0, 8));
+                const float4 x1 = *reinterpret_cast<const float4*>(src + chunk_off(row, 1, 8));
+                sum[0] += x0.x; sum[1] += x0.y; sum[2] += x0.z; sum[3] += x0.w;
+                sum[4] += x1.x; sum[5] += x1.y; sum[6] += x1.z; sum[7] += x1.w;
+              }
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) sum[j] = lin(sum[j], lcs, lcb);
+            if (lact) {
+#pragma unroll
+              for (int j = 0; j < 8; ++j) sum[j] = gelu_tanh(sum[j]);
+            }
+            uint8_t* buf = wbuf + ((lc * 8) >> 5) * kWarpOutBytes;
+            const int r0 = (lc * 8) & 31;
+            const int cb = lane * 2;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const int rr = r0 + j;
+              *reinterpret_cast<__nv_bfloat16*>(buf + rr * 64 + (((cb >> 4) ^ ((rr >> 1) & 3)) << 4) +
+                                                (cb & 15)) = __float2bfloat16_rn(sum[j]);
+            }
           }
-          // partial sums added in rank order, this CTA's own at its rank
-          float sum[32];
+          dev::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            for (int lc = 0; lc < owned; ++lc)
+              dev::tma_store_2d(&tmap_out,
+                                wbuf_s + ((lc * 8) >> 5) * kWarpOutBytes + ((lc * 8) & 31) * 64,
+                                tn * kTile + ew * 32, tm * kBN + (own_c0 + lc) * 8);
+            dev::bulk_commit();
+          }
+        } else {
+          for (int c = own_c0; c < own_c1; ++c) {
+            const int lc = c - own_c0;
+            float acc[32];
+            dev::tmem_ld32(tacc + c * 32, acc);
+            // partial sums added in rank order, this CTA's own at its rank
+            float sum[32];
 #pragma unroll
-          for (int j = 0; j < 32; ++j) sum[j] = 0.0f;
-          for (int r = 0; r < S; ++r) {
-            if (r == rank) {
+            for (int j = 0; j < 32; ++j) sum[j] = 0.0f;
+            for (int r = 0; r < S; ++r) {
+              if (r == rank) {
 #pragma unroll
-              for (int j = 0; j < 32; ++j) sum[j] += acc[j];
-            } else {
-              const int slot = r < rank ? r : r - 1;
-              const uint8_t* src = recv + (slot * owned_max + lc) * chunk_bytes;
+                for (int j = 0; j < 32; ++j) sum[j] += acc[j];
+              } else {
+                const int slot = r < rank ? r : r - 1;
+                const uint8_t* src = recv + (slot * owned_max + lc) * chunk_bytes;
 #pragma unroll
-              for (int q = 0; q < 8; ++q) {
-                if (4 * q < CW) {
-                  const float4 x = *reinterpret_cast<const float4*>(src + chunk_off(row, q, CW));
+                for (int q = 0; q < 8; ++q) {
+                  const float4 x = *reinterpret_cast<const float4*>(src + chunk_off(row, q, 32));
                   sum[4 * q] += x.x;
                   sum[4 * q + 1] += x.y;
                   sum[4 * q + 2] += x.z;
@@ -538,19 +619,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
               }
             }
-          }
-          if constexpr (!kSwap) {
             finish32(sum, c * 32, 0);
-          } else {
-#pragma unroll
-            for (int j = 0; j < 8; ++j) sum[j] = lin(sum[j], lcs, lcb);
-            if (lact) {
-#pragma unroll
-              for (int j = 0; j < 8; ++j) sum[j] = gelu_tanh(sum[j]);
-            }
-            warp_store<true, 8>(sum, wbuf + wb * kWarpOutBytes, wbuf_s + wb * kWarpOutBytes,
-                                &tmap_out, tn * kTile + ew * 32, tm * kBN + c * 8, lane);
-            wb ^= 1;
           }
         }
       }
