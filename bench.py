@@ -360,7 +360,7 @@ def run_headline(args, device, world, sampler, peaks, peak_kind):
     roofline = {"bound": "tensor", "achieved": achieved, "peak": fp8_peak, "unit": "TFLOP/s",
                 "frac": achieved / fp8_peak, "traffic": traffic,
                 "traffic_unit": "bytes per launch (mean over the step's 3 GEMM launches, ncu)",
-                "kernel": "gemm_tc_kernel<fp8, 128x256 tiles>",
+                "kernel": "gemm_tc_kernel<fp8, CTA-pair 256x128 / 256x256 tiles>",
                 "peak_source": "%s bf16 sustained x %.0f (nominal FP8/BF16 dense ratio), of %s"
                                % (peak_kind, FP8_OVER_BF16, peak_kind),
                 "per_launch_flops": tot_flops / len(set0.layers)}

@@ -56,6 +56,7 @@ constexpr int kTile = 128;               // MMA M; channels per packed weight ti
 constexpr int kKBytes = 128;             // bytes of K per pipeline stage
 constexpr int kWTile = kTile * kKBytes;  // bytes of one packed weight tile
 constexpr int kSmemMax = 232448;         // dynamic shared memory limit per CTA
+constexpr int kPairMinSmem = 200 * 1024;  // shared memory floor of a pair CTA
 constexpr int kWarpOutBytes = 2048;      // one warp's bf16 output staging buffer
 constexpr int kOutBytes = 4 * 2 * kWarpOutBytes;  // 4 epilogue warps x 2 buffers
 constexpr int kBarRegion = 512;          // mbarriers, TMEM address, abort flag
@@ -83,17 +84,26 @@ struct GemmArgs {
   int* dev_status;
 };
 
-template <bool kSwap, int kBN>
+template <bool kSwap, bool kPair, int kBN>
 struct Cfg {
   static constexpr int kActRows = kSwap ? kBN : kTile;
-  static constexpr int kWRows = kSwap ? kTile : kBN;
+  // a pair's CTAs each hold half of the tile's weight channels
+  static constexpr int kWRows = kSwap ? kTile : (kPair ? kBN / 2 : kBN);
   static constexpr int kActBytes = kActRows * kKBytes;
   static constexpr int kWBytes = kWRows * kKBytes;
   static constexpr int kStageBytes = kActBytes + kWBytes;
-  static constexpr int kTmemCols = 2 * kBN;  // two accumulator buffers
+  // output rows of a large-M tile: 128, or 256 for a CTA pair
+  static constexpr int kTileRows = kPair ? 2 * kTile : kTile;
+  // two accumulator buffers, so that a tile's epilogue overlaps the next
+  // tile's mainloop (a pair's 256-column tiles take all 512 TMEM columns;
+  // the host gives such a CTA enough shared memory that no other CTA that
+  // allocates TMEM is resident beside it)
+  static constexpr int kAccBufs = 2;
+  static constexpr int kTmemCols = kAccBufs * kBN;
   static_assert(kActBytes % 1024 == 0 && kWBytes % 1024 == 0, "operand tiles 1024-aligned");
   static_assert(kBN == 32 || kBN == 64 || kBN == 128 || kBN == 256, "tile width");
   static_assert(kSwap || kBN >= 128, "large-M tiles are 128 x 128 or 128 x 256");
+  static_assert(!(kSwap && kPair), "CTA pairs take large-M tiles");
 };
 
 // tanh-GELU, 0.5 v (1 + tanh(u)) with u = sqrt(2/pi) (v + 0.044715 v^3),
@@ -160,11 +170,12 @@ __device__ __forceinline__ uint32_t chunk_off(int r, int q, int cw) {
   return static_cast<uint32_t>(r * cw * 4 + ((q ^ swz) << 4));
 }
 
-template <bool kFp8, bool kSwap, int kBN>
+template <bool kFp8, bool kSwap, bool kPair, int kBN>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_act,
+                   const __grid_constant__ CUtensorMap tmap_w,
                    const __grid_constant__ CUtensorMap tmap_out, const GemmArgs p) {
-  using C = Cfg<kSwap, kBN>;
+  using C = Cfg<kSwap, kPair, kBN>;
   constexpr int kEsize = kFp8 ? 1 : 2;
   const int stages = p.stages;
   extern __shared__ uint8_t smem_raw[];
@@ -185,7 +196,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x & 31;
   const bool split = p.splits > 1;
   const int S = p.splits;
-  const int rank = split ? static_cast<int>(dev::cluster_ctarank()) : 0;
+  // cluster layout: a pair's two CTAs along x, split-K ranks along z
+  const uint32_t crank = (kPair || split) ? dev::cluster_ctarank() : 0u;
+  const int px = kPair ? static_cast<int>(crank & 1u) : 0;  // CTA within the pair
+  const int rank = kPair ? static_cast<int>(crank >> 1) : static_cast<int>(crank);  // K split
+  const bool leader = px == 0;  // issues the pair's MMAs
+  const uint32_t lead_rank = crank & ~1u;
+  // cluster rank of the CTA that holds K split j of this CTA's rows
+  auto split_cta = [&](int j) -> uint32_t {
+    return kPair ? static_cast<uint32_t>(2 * j + px) : static_cast<uint32_t>(j);
+  };
 
   // split-K chunks: chunk_cols TMEM columns each; rank j owns chunks
   // [cb(j), cb(j+1)) with cb(j) = ceil(j * NC / S)
@@ -204,8 +224,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     dev::mbar_init(tfull0, 1);
     dev::mbar_init(tfull0 + 8, 1);
-    dev::mbar_init(tempty0, 4);
-    dev::mbar_init(tempty0 + 8, 4);
+    // accumulator released by every epilogue warp (of both CTAs of a pair)
+    dev::mbar_init(tempty0, kPair ? 8 : 4);
+    dev::mbar_init(tempty0 + 8, kPair ? 8 : 4);
     dev::mbar_init(recv_bar, 1);
     *abort_flag = 0;
     dev::fence_mbar_init();
@@ -214,9 +235,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                static_cast<uint32_t>(own_c1 - own_c0) *
                                                chunk_bytes);
     dev::prefetch_tmap(&tmap_act);
+    if (kPair) dev::prefetch_tmap(&tmap_w);
     dev::prefetch_tmap(&tmap_out);
   }
-  if (warp == 1) dev::tmem_alloc(dev::smem_u32(tmem_slot), C::kTmemCols);
+  if (warp == 1) {
+    if constexpr (kPair)
+      dev::tmem_alloc_pair(dev::smem_u32(tmem_slot), C::kTmemCols);
+    else
+      dev::tmem_alloc(dev::smem_u32(tmem_slot), C::kTmemCols);
+  }
   dev::tc_fence_before();
   __syncthreads();
   dev::tc_fence_after();
@@ -224,6 +251,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   // the next grid on the stream may start its prologue (it waits for this
   // grid's completion before it reads or writes anything this grid touches)
   dev::grid_launch_dependents();
+  // a pair signals mbarriers across its two CTAs from the first copy on:
+  // both CTAs' barriers are initialised before either goes on.  (Every
+  // cluster-barrier arrive and wait in this kernel is executed by all 32
+  // lanes of a warp together.)
+  if constexpr (kPair) {
+    dev::cluster_arrive();
+    dev::cluster_wait();
+  }
   // Split-K cluster barrier, phase 1: with dedicated receive buffers every
   // thread arrives now (its mbarriers are initialised); when the receive
   // buffers reuse the stage buffers, each thread arrives once this CTA's
@@ -231,13 +266,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (split && !p.recv_in_stages) dev::cluster_arrive_relaxed();
 
   // this CTA's tiles: split -> one tile and a K range; else a strided list
+  // (a pair walks its list together)
   const int kb0 = split ? rank * p.kb_per_split : 0;
   const int nkb = split ? min(p.kb_per_split, p.kb_total - kb0) : p.kb_total;
-  const int t_step = split ? p.num_tiles : static_cast<int>(gridDim.x);
-  const int my_tiles =
-      split ? 1 : (p.num_tiles - static_cast<int>(blockIdx.x) + t_step - 1) / t_step;
+  const int first_tile = kPair ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int t_step = split ? p.num_tiles : static_cast<int>(kPair ? gridDim.x >> 1 : gridDim.x);
+  const int my_tiles = split ? 1 : (p.num_tiles - first_tile + t_step - 1) / t_step;
   auto tile_of = [&](int it, int& tm, int& tn) {
-    const int t = static_cast<int>(blockIdx.x) + it * t_step;
+    const int t = first_tile + it * t_step;
     if (kSwap) {
       tn = t % p.tiles_n;
       tm = t / p.tiles_n;
@@ -257,29 +293,57 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto geom = [&](int g, int& tm, int& nbf, int& groups) -> uint32_t {
         int tn;
         tile_of(g / nkb, tm, tn);
+        if constexpr (kPair) {
+          // 256-channel tiles: one 128-channel group per CTA; 128-channel
+          // tiles: one half group per CTA.  Both CTAs' copies complete on
+          // the leader's barrier.
+          nbf = kBN == 256 ? 2 * tn + px : tn;
+          groups = 1;
+          return static_cast<uint32_t>(2 * C::kStageBytes);
+        }
         nbf = kSwap ? tn : tn * (kBN / kTile);
         groups = kSwap ? 1 : min(kBN / kTile, p.nb_total - nbf);
         return static_cast<uint32_t>(C::kActBytes + groups * kWTile);
       };
+      // the stage's full barrier: a pair's is the leader's
+      auto full_bar = [&](int s) -> uint32_t {
+        return kPair ? dev::map_to_rank(full0 + 8 * s, lead_rank) : full0 + 8 * s;
+      };
+      auto arm = [&](int s, uint32_t tx) {
+        if (!kPair || leader) dev::mbar_arrive_expect_tx(full0 + 8 * s, tx);
+      };
       auto load_weights = [&](int g, int s, int nbf, int groups) {
         const uint32_t st = sbase + s * C::kStageBytes;
         const int kb = kb0 + g % nkb;
-        for (int q = 0; q < groups; ++q) {
-          const uint8_t* src =
-              p.w_packed + (static_cast<size_t>(nbf + q) * p.kb_total + kb) * kWTile;
-          dev::bulk_load(st + C::kActBytes + q * kWTile, src, kWTile, full0 + 8 * s, pol_w);
+        if constexpr (kPair) {
+          // packed tiles seen as rows of 128 bytes; rows past the weight
+          // (channels >= N) arrive as zeros
+          const int half = kBN == 256 ? 0 : px;
+          dev::tma_load_2d_pair(st + C::kActBytes, &tmap_w, 0,
+                                (nbf * p.kb_total + kb) * kTile + half * (kTile / 2), full_bar(s),
+                                pol_w);
+        } else {
+          for (int q = 0; q < groups; ++q) {
+            const uint8_t* src =
+                p.w_packed + (static_cast<size_t>(nbf + q) * p.kb_total + kb) * kWTile;
+            dev::bulk_load(st + C::kActBytes + q * kWTile, src, kWTile, full0 + 8 * s, pol_w);
+          }
         }
       };
       auto load_act = [&](int g, int s, int tm) {
-        dev::tma_load_2d(sbase + s * C::kStageBytes, &tmap_act,
-                         (kb0 + g % nkb) * (kKBytes / kEsize), tm * C::kActRows, full0 + 8 * s,
-                         pol_a);
+        const int x = (kb0 + g % nkb) * (kKBytes / kEsize);
+        if constexpr (kPair)
+          dev::tma_load_2d_pair(sbase + s * C::kStageBytes, &tmap_act, x,
+                                tm * C::kTileRows + px * kTile, full_bar(s), pol_a);
+        else
+          dev::tma_load_2d(sbase + s * C::kStageBytes, &tmap_act, x, tm * C::kActRows,
+                           full0 + 8 * s, pol_a);
       };
       const int npre = total < stages ? total : stages;
       for (int g = 0; g < npre; ++g) {  // first use of each stage needs no wait
         int tm, nbf, groups;
         const uint32_t tx = geom(g, tm, nbf, groups);
-        dev::mbar_arrive_expect_tx(full0 + 8 * g, tx);
+        arm(g, tx);
         load_weights(g, g, nbf, groups);
       }
       dev::grid_dependency_wait();
@@ -297,7 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         int tm, nbf, groups;
         const uint32_t tx = geom(g, tm, nbf, groups);
-        dev::mbar_arrive_expect_tx(full0 + 8 * s, tx);
+        arm(s, tx);
         load_weights(g, s, nbf, groups);
         load_act(g, s, tm);
         issued = g + 1;
@@ -307,24 +371,42 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       // Do not leave with copies in flight: wait (bounded, even after an
-      // abort) for the last use of every stage that was armed.
-      for (int g = issued - stages < 0 ? 0 : issued - stages; g < issued; ++g)
-        dev::mbar_wait(full0 + 8 * (g % stages), (g / stages) & 1, nullptr, p.dev_status,
-                       dev::kTimeoutProducer);
+      // abort) for the last use of every stage that was armed.  A pair's
+      // copies complete on the leader's barriers, so each of its CTAs waits
+      // instead until the MMAs released its stages (which also means the
+      // leader's commits to this CTA's barriers have landed).
+      for (int g = issued - stages < 0 ? 0 : issued - stages; g < issued; ++g) {
+        if constexpr (kPair)
+          dev::mbar_wait(empty0 + 8 * (g % stages), (g / stages) & 1, nullptr, p.dev_status,
+                         dev::kTimeoutProducer);
+        else
+          dev::mbar_wait(full0 + 8 * (g % stages), (g / stages) & 1, nullptr, p.dev_status,
+                         dev::kTimeoutProducer);
+      }
     }
     __syncwarp();
   } else if (warp == 1) {
-    if (lane == 0) {
+    if (lane == 0 && leader) {
       // ------------------------------------------------------------ MMA
-      constexpr uint32_t idesc = dev::instr_desc(kFp8, kTile, kBN);
+      constexpr uint32_t idesc = dev::instr_desc(kFp8, C::kTileRows, kBN);
+      const uint16_t pair_mask = static_cast<uint16_t>(3u << lead_rank);
+      auto commit = [&](uint32_t bar) {
+        if constexpr (kPair)
+          dev::mma_commit_pair(bar, pair_mask);  // both CTAs' barriers at this offset
+        else
+          dev::mma_commit(bar);
+      };
       int s = 0;
       uint32_t ph = 0;
       for (int it = 0; it < my_tiles; ++it) {
-        const int b = it & 1;
-        const uint32_t u = static_cast<uint32_t>(it >> 1);
-        if (!dev::mbar_wait(tempty0 + 8 * b, (u & 1) ^ 1, abort_flag, p.dev_status,
-                            dev::kTimeoutMma))
-          break;
+        const int b = it % C::kAccBufs;
+        const uint32_t u = static_cast<uint32_t>(it / C::kAccBufs);
+        const bool free_acc =
+            kPair ? dev::mbar_wait_cluster(tempty0 + 8 * b, (u & 1) ^ 1, abort_flag, p.dev_status,
+                                           dev::kTimeoutMma)
+                  : dev::mbar_wait(tempty0 + 8 * b, (u & 1) ^ 1, abort_flag, p.dev_status,
+                                   dev::kTimeoutMma);
+        if (!free_acc) break;
         dev::tc_fence_after();
         const uint32_t d = tmem + static_cast<uint32_t>(b * kBN);
         bool stop = false;
@@ -341,15 +423,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t ad = dev::smem_desc_sw128(a_addr);
           const uint64_t bd = dev::smem_desc_sw128(b_addr);
 #pragma unroll
-          for (int k = 0; k < kKBytes / 32; ++k)
-            dev::mma<kFp8>(d, ad + 2 * k, bd + 2 * k, idesc, (i | k) != 0);
-          dev::mma_commit(empty0 + 8 * s);
+          for (int k = 0; k < kKBytes / 32; ++k) {
+            if constexpr (kPair)
+              dev::mma_pair<kFp8>(d, ad + 2 * k, bd + 2 * k, idesc, (i | k) != 0);
+            else
+              dev::mma<kFp8>(d, ad + 2 * k, bd + 2 * k, idesc, (i | k) != 0);
+          }
+          commit(empty0 + 8 * s);
           if (++s == stages) {
             s = 0;
             ++ph;
           }
         }
-        dev::mma_commit(tfull0 + 8 * b);
+        commit(tfull0 + 8 * b);
         if (stop) break;
       }
     }
@@ -364,11 +450,33 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t wbuf_s = sbase + p.outbuf_off + (warp - 2) * 2 * kWarpOutBytes;
     int wb = 0;
     bool ok = true;
+    // a drained accumulator buffer goes back to the MMA issuer (the leader
+    // of a pair, whose MMAs write both CTAs' TMEM)
+    auto release_acc = [&](int b) {
+      dev::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if constexpr (kPair)
+          dev::mbar_arrive_cluster(dev::map_to_rank(tempty0 + 8 * b, lead_rank));
+        else
+          dev::mbar_arrive(tempty0 + 8 * b);
+      }
+    };
     for (int it = 0; it < my_tiles; ++it) {
       int tm, tn;
       tile_of(it, tm, tn);
-      const int b = it & 1;
-      const uint32_t u = static_cast<uint32_t>(it >> 1);
+      const int b = it % C::kAccBufs;
+      const uint32_t u = static_cast<uint32_t>(it / C::kAccBufs);
+      // per-channel weight scale and bias are load-time data: fetch them
+      // while the MMAs run
+      constexpr int kColsPerThread = kSwap ? 1 : kBN / 128;
+      float wsc[kColsPerThread], wbi[kColsPerThread];
+#pragma unroll
+      for (int j = 0; j < kColsPerThread; ++j) {
+        const int n = kSwap ? tn * kTile + row : tn * kBN + et + 128 * j;
+        wsc[j] = n < p.N ? (p.w_scale ? __ldg(p.w_scale + n) : 1.0f) : 0.0f;
+        wbi[j] = (n < p.N && p.bias) ? __ldg(p.bias + n) : 0.0f;
+      }
       ok = dev::mbar_wait(tfull0 + 8 * b, u & 1, abort_flag, p.dev_status,
                           dev::kTimeoutEpilogue);
       ok = __all_sync(0xffffffffu, ok);
@@ -378,25 +486,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       // (after the MMAs consumed activations loaded after the dependency
       // wait) and through L2
       const float as = p.a_scale ? __ldcg(p.a_scale) : 1.0f;
-      float* cs_s = col_sb + b * 2 * kBN;  // per-channel scale and bias of the tile
+      float* cs_s = col_sb + (it & 1) * 2 * kBN;  // per-channel scale and bias of the tile
       float* cb_s = cs_s + kBN;
       float lcs = 1.0f, lcb = 0.0f;
       bool lact = false;
       if constexpr (!kSwap) {
-        for (int c = et; c < kBN; c += 128) {
-          const int n = tn * kBN + c;
-          cs_s[c] = n < p.N ? as * (p.w_scale ? __ldg(p.w_scale + n) : 1.0f) : 0.0f;
-          cb_s[c] = (n < p.N && p.bias) ? __ldg(p.bias + n) : 0.0f;
+#pragma unroll
+        for (int j = 0; j < kColsPerThread; ++j) {
+          cs_s[et + 128 * j] = as * wsc[j];
+          cb_s[et + 128 * j] = wbi[j];
         }
         dev::named_sync(1, 128);
       } else {
         const int n = tn * kTile + row;
         if (n < p.N) {
-          lcs = as * (p.w_scale ? __ldg(p.w_scale + n) : 1.0f);
-          lcb = p.bias ? __ldg(p.bias + n) : 0.0f;
+          lcs = as * wsc[0];
+          lcb = wbi[0];
           lact = n < p.act_cols;
         }
       }
+      const int row0 = tm * C::kTileRows + px * kTile;  // large M: first output row of this CTA
       // epilogue of 32 accumulator columns starting at tile column c32, and
       // this warp's store of them
       auto finish32 = [&](float* v, int c32, int rows_of_tile_m0) {
@@ -419,7 +528,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (n0 + j < p.act_cols) v[j] = gelu_tanh(v[j]);
           }
           warp_store<false, 32>(v, wbuf + wb * kWarpOutBytes, wbuf_s + wb * kWarpOutBytes,
-                                &tmap_out, n0, tm * kTile + ew * 32, lane);
+                                &tmap_out, n0, row0 + ew * 32, lane);
         } else {
 #pragma unroll
           for (int j = 0; j < 32; ++j) v[j] = lin(v[j], lcs, lcb);
@@ -439,20 +548,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int c = 0; c < kBN; c += 64) {
             float v[64];
             dev::tmem_ld64(tacc + c, v);
-            if (c + 64 == kBN) {  // accumulator buffer free for the tile after next
-              dev::tc_fence_before();
-              __syncwarp();
-              if (lane == 0) dev::mbar_arrive(tempty0 + 8 * b);
-            }
+            if (c + 64 == kBN) release_acc(b);  // accumulator read out
             finish32(v, c, tm * kBN);
             finish32(v + 32, c + 32, tm * kBN);
           }
         } else {
           float v[32];
           dev::tmem_ld32(tacc, v);
-          dev::tc_fence_before();
-          __syncwarp();
-          if (lane == 0) dev::mbar_arrive(tempty0 + 8 * b);
+          release_acc(b);
           finish32(v, 0, tm * kBN);
         }
       } else {
@@ -529,10 +632,11 @@ __global__ void __launch_bounds__(kThreads, 1)
               const int sp0 = oc0 < own_c0 ? oc0 : oc0 - owned;
               const int slot = rank < o ? rank : rank - 1;
               const uint32_t dst = dev::map_to_rank(
-                  sbase + p.recv_off + static_cast<uint32_t>(slot * owned_max) * chunk_bytes, o);
+                  sbase + p.recv_off + static_cast<uint32_t>(slot * owned_max) * chunk_bytes,
+                  split_cta(o));
               dev::bulk_copy_to_peer(dst, sbase + sp0 * chunk_bytes,
                                      static_cast<uint32_t>(oc1 - oc0) * chunk_bytes,
-                                     dev::map_to_rank(recv_bar, o));
+                                     dev::map_to_rank(recv_bar, split_cta(o)));
             }
           }
         }
@@ -637,12 +741,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     // phase 2: every CTA has received its chunks, so no copy out of this
     // CTA's shared memory is still in flight
     dev::cluster_wait();
+  } else if constexpr (kPair) {
+    // neither CTA of a pair leaves (or frees TMEM) while the other may still
+    // take part in its MMAs or signal its barriers
+    dev::cluster_arrive();
+    dev::cluster_wait();
   }
   dev::tc_fence_before();
   __syncthreads();
   if (warp == 1) {
     dev::tc_fence_after();
-    dev::tmem_dealloc(tmem, C::kTmemCols);
+    if constexpr (kPair)
+      dev::tmem_dealloc_pair(tmem, C::kTmemCols);
+    else
+      dev::tmem_dealloc(tmem, C::kTmemCols);
   }
 }
 
@@ -666,6 +778,7 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 // the same plan): tile kind and width, split-K factor, grid, pipeline depth.
 struct Plan {
   bool swap;
+  bool pair;  // 256-row tiles on CTA pairs (cta_group::2)
   int bn;
   int tiles_m, tiles_n, num_tiles;
   int splits;
@@ -706,7 +819,7 @@ bool layout(Plan& pl, int stage_bytes) {
 }
 
 // Sets the kernel's dynamic shared memory limit once per device.
-template <bool kFp8, bool kSwap, int kBN>
+template <bool kFp8, bool kSwap, bool kPair, int kBN>
 cudaError_t prepare_kernel() {
   static std::mutex mu;
   static bool attr_set[64] = {false};
@@ -714,7 +827,7 @@ cudaError_t prepare_kernel() {
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(mu);
   if (!attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<kFp8, kSwap, kBN>,
+    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<kFp8, kSwap, kPair, kBN>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
@@ -722,16 +835,17 @@ cudaError_t prepare_kernel() {
   return cudaSuccess;
 }
 
-// Number of clusters of `s` CTAs with `smem` bytes each that can be resident
-// at once (cached per device and configuration).
-template <bool kFp8, bool kSwap, int kBN>
+// Number of clusters of `s` split-K CTAs (times 2 for pairs) with `smem`
+// bytes each that can be resident at once (cached per device and
+// configuration).
+template <bool kFp8, bool kSwap, bool kPair, int kBN>
 int cluster_capacity(int s, int smem) {
   static std::mutex mu;
   static int cache[64][kMaxSplits + 1][8];
   static bool init = false;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-  if (prepare_kernel<kFp8, kSwap, kBN>() != cudaSuccess) return 0;
+  if (prepare_kernel<kFp8, kSwap, kPair, kBN>() != cudaSuccess) return 0;
   const int sb = (smem + 32767) / 32768;  // smem bucket of 32 KiB
   std::lock_guard<std::mutex> lock(mu);
   if (!init) {
@@ -743,19 +857,20 @@ int cluster_capacity(int s, int smem) {
   int& c = cache[dev][s][sb < 8 ? sb : 7];
   if (c < 0) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(1, 1, static_cast<unsigned>(s));
+    cfg.gridDim = dim3(kPair ? 2 : 1, 1, static_cast<unsigned>(s));
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = static_cast<size_t>(sb < 8 ? sb * 32768 : kSmemMax);
     if (cfg.dynamicSmemBytes > static_cast<size_t>(kSmemMax)) cfg.dynamicSmemBytes = kSmemMax;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.x = kPair ? 2 : 1;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = static_cast<unsigned>(s);
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<kFp8, kSwap, kBN>, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<kFp8, kSwap, kPair, kBN>, &cfg) !=
+        cudaSuccess) {
       cudaGetLastError();
       n = 0;
     }
@@ -765,14 +880,17 @@ int cluster_capacity(int s, int smem) {
 }
 
 template <bool kFp8>
-int cluster_capacity_for(bool swap, int bn, int s, int smem) {
-  if (!swap)
-    return bn == 128 ? cluster_capacity<kFp8, false, 128>(s, smem)
-                     : cluster_capacity<kFp8, false, 256>(s, smem);
-  switch (bn) {
-    case 32: return cluster_capacity<kFp8, true, 32>(s, smem);
-    case 64: return cluster_capacity<kFp8, true, 64>(s, smem);
-    default: return cluster_capacity<kFp8, true, 128>(s, smem);
+int cluster_capacity_for(const Plan& pl, int s, int smem) {
+  if (pl.pair)
+    return pl.bn == 128 ? cluster_capacity<kFp8, false, true, 128>(s, smem)
+                        : cluster_capacity<kFp8, false, true, 256>(s, smem);
+  if (!pl.swap)
+    return pl.bn == 128 ? cluster_capacity<kFp8, false, false, 128>(s, smem)
+                        : cluster_capacity<kFp8, false, false, 256>(s, smem);
+  switch (pl.bn) {
+    case 32: return cluster_capacity<kFp8, true, false, 32>(s, smem);
+    case 64: return cluster_capacity<kFp8, true, false, 64>(s, smem);
+    default: return cluster_capacity<kFp8, true, false, 128>(s, smem);
   }
 }
 
@@ -813,6 +931,8 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int esize, bool fp8) {
   Plan pl;
   const int kb = static_cast<int>(ceil_div(K * esize, kKBytes));
   const int nb = static_cast<int>(ceil_div(N, kTile));
+  const int sms = sm_count() > 0 ? sm_count() : 148;
+  pl.pair = false;
   if (M <= 128) {
     pl.swap = true;
     pl.bn = M <= 32 ? 32 : (M <= 64 ? 64 : 128);
@@ -820,29 +940,31 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int esize, bool fp8) {
     pl.tiles_m = static_cast<int>(ceil_div(M, pl.bn));
     pl.chunk_cols = 8;
   } else {
-    // 128 x 256 tiles carry the most FLOPs per byte a CTA ingests; when they
-    // would leave most SMs idle on a short K loop, 128 x 128 tiles fill the
-    // machine without a split-K exchange
+    // 256-row tiles on CTA pairs: each CTA ingests 128 activation rows and
+    // half of the tile's weight channels per k-block.  256 x 256 tiles carry
+    // the most FLOPs per ingested byte; when they would leave most SMs idle
+    // on a short K loop, 256 x 128 tiles fill the machine without a split-K
+    // exchange.
     pl.swap = false;
-    pl.tiles_m = static_cast<int>(ceil_div(M, kTile));
-    const int sms0 = sm_count() > 0 ? sm_count() : 148;
-    const int64_t wide = pl.tiles_m * ceil_div(N, 256);
-    const int64_t narrow = pl.tiles_m * ceil_div(N, 128);
-    pl.bn = (2 * wide <= sms0 && narrow <= sms0 && kb <= 32) ? 128 : 256;
+    pl.pair = true;
+    pl.tiles_m = static_cast<int>(ceil_div(M, 2 * kTile));
+    const int64_t wide = 2 * pl.tiles_m * ceil_div(N, 256);  // CTAs
+    const int64_t narrow = 2 * pl.tiles_m * ceil_div(N, 128);
+    pl.bn = (2 * wide <= sms && narrow <= sms && kb <= 32) ? 128 : 256;
     pl.tiles_n = static_cast<int>(ceil_div(N, pl.bn));
     pl.chunk_cols = 32;
   }
   pl.num_tiles = pl.tiles_m * pl.tiles_n;
-  const int sms = sm_count() > 0 ? sm_count() : 148;
+  const int ctas_per_tile = pl.pair ? 2 : 1;
   const int act_rows = pl.swap ? pl.bn : kTile;
-  const int w_rows = pl.swap ? kTile : pl.bn;
+  const int w_rows = pl.swap ? kTile : (pl.pair ? pl.bn / 2 : pl.bn);
   const int stage_bytes = (act_rows + w_rows) * kKBytes;
 
   int s_max = 1;
-  if (pl.num_tiles < sms) {
-    s_max = sms / pl.num_tiles;
+  if (pl.num_tiles * ctas_per_tile < sms) {
+    s_max = sms / (pl.num_tiles * ctas_per_tile);
     const int nchunks = pl.bn / pl.chunk_cols;
-    if (s_max > kMaxSplits) s_max = kMaxSplits;
+    if (s_max > kMaxSplits / ctas_per_tile) s_max = kMaxSplits / ctas_per_tile;
     if (s_max > nchunks) s_max = nchunks;
     if (s_max > kb) s_max = kb;
     if (s_max < 1) s_max = 1;
@@ -861,22 +983,32 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int esize, bool fp8) {
     }
     if (!place_buffers(pl, stage_bytes, want)) continue;
     if (pl.splits == 1) break;
-    const int capacity = fp8 ? cluster_capacity_for<true>(pl.swap, pl.bn, pl.splits, pl.smem)
-                             : cluster_capacity_for<false>(pl.swap, pl.bn, pl.splits, pl.smem);
+    const int smem = pl.pair && pl.smem < kPairMinSmem ? kPairMinSmem : pl.smem;
+    const int capacity = fp8 ? cluster_capacity_for<true>(pl, pl.splits, smem)
+                             : cluster_capacity_for<false>(pl, pl.splits, smem);
     if (capacity >= pl.num_tiles) break;
   }
-  if (pl.splits > 1)
-    pl.grid = dim3(static_cast<unsigned>(pl.num_tiles), 1, static_cast<unsigned>(pl.splits));
-  else
-    pl.grid = dim3(static_cast<unsigned>(pl.num_tiles < sms ? pl.num_tiles : sms), 1, 1);
+  // a pair CTA takes all 512 TMEM columns: with at least kPairMinSmem of
+  // shared memory no other GEMM CTA (each takes over 40 KiB) is resident
+  // beside it, while the small CTAs of other kernels still are
+  if (pl.pair && pl.smem < kPairMinSmem) pl.smem = kPairMinSmem;
+  if (pl.splits > 1) {
+    pl.grid = dim3(static_cast<unsigned>(pl.num_tiles * ctas_per_tile), 1,
+                   static_cast<unsigned>(pl.splits));
+  } else {
+    const int units = sms / ctas_per_tile;  // persistent: one CTA (pair) per SM (two SMs)
+    pl.grid = dim3(static_cast<unsigned>((pl.num_tiles < units ? pl.num_tiles : units) *
+                                         ctas_per_tile),
+                   1, 1);
+  }
   return pl;
 }
 
-template <bool kFp8, bool kSwap, int kBN>
-cudaError_t launch_one(const CUtensorMap& ta, const CUtensorMap& to, const GemmArgs& a,
-                       const Plan& pl, cudaStream_t stream) {
-  auto kern = gemm_tc_kernel<kFp8, kSwap, kBN>;
-  cudaError_t e = prepare_kernel<kFp8, kSwap, kBN>();
+template <bool kFp8, bool kSwap, bool kPair, int kBN>
+cudaError_t launch_one(const CUtensorMap& ta, const CUtensorMap& tw, const CUtensorMap& to,
+                       const GemmArgs& a, const Plan& pl, cudaStream_t stream) {
+  auto kern = gemm_tc_kernel<kFp8, kSwap, kPair, kBN>;
+  cudaError_t e = prepare_kernel<kFp8, kSwap, kPair, kBN>();
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = pl.grid;
@@ -887,24 +1019,27 @@ cudaError_t launch_one(const CUtensorMap& ta, const CUtensorMap& to, const GemmA
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   attr[1].id = cudaLaunchAttributeClusterDimension;
-  attr[1].val.clusterDim.x = 1;
+  attr[1].val.clusterDim.x = kPair ? 2 : 1;
   attr[1].val.clusterDim.y = 1;
   attr[1].val.clusterDim.z = pl.splits;
   cfg.attrs = attr;
-  cfg.numAttrs = pl.splits > 1 ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, kern, ta, to, a);
+  cfg.numAttrs = (kPair || pl.splits > 1) ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, kern, ta, tw, to, a);
 }
 
 template <bool kFp8>
-cudaError_t dispatch(const CUtensorMap& ta, const CUtensorMap& to, const GemmArgs& a,
-                     const Plan& pl, cudaStream_t stream) {
+cudaError_t dispatch(const CUtensorMap& ta, const CUtensorMap& tw, const CUtensorMap& to,
+                     const GemmArgs& a, const Plan& pl, cudaStream_t stream) {
+  if (pl.pair)
+    return pl.bn == 128 ? launch_one<kFp8, false, true, 128>(ta, tw, to, a, pl, stream)
+                        : launch_one<kFp8, false, true, 256>(ta, tw, to, a, pl, stream);
   if (!pl.swap)
-    return pl.bn == 128 ? launch_one<kFp8, false, 128>(ta, to, a, pl, stream)
-                        : launch_one<kFp8, false, 256>(ta, to, a, pl, stream);
+    return pl.bn == 128 ? launch_one<kFp8, false, false, 128>(ta, tw, to, a, pl, stream)
+                        : launch_one<kFp8, false, false, 256>(ta, tw, to, a, pl, stream);
   switch (pl.bn) {
-    case 32: return launch_one<kFp8, true, 32>(ta, to, a, pl, stream);
-    case 64: return launch_one<kFp8, true, 64>(ta, to, a, pl, stream);
-    default: return launch_one<kFp8, true, 128>(ta, to, a, pl, stream);
+    case 32: return launch_one<kFp8, true, false, 32>(ta, tw, to, a, pl, stream);
+    case 64: return launch_one<kFp8, true, false, 64>(ta, tw, to, a, pl, stream);
+    default: return launch_one<kFp8, true, false, 128>(ta, tw, to, a, pl, stream);
   }
 }
 
@@ -929,11 +1064,15 @@ frt_status gemm_common(bool fp8, const void* a, int64_t lda, const float* a_scal
       (bias && !aligned(bias, 4)) || (dev_status && !aligned(dev_status, 4)))
     return FRT_ERR_MISALIGNED;
 
+  const int64_t kb_total = ceil_div(K * esize, kKBytes);
+  const int64_t nb_total = ceil_div(N, kTile);
+  if (nb_total * kb_total * kTile > (1LL << 31) - 1) return FRT_ERR_UNSUPPORTED_SHAPE;
+
   auto encode = tensor_map_encoder();
   if (!encode) return FRT_ERR_CUDA;
   const Plan pl = make_plan(M, N, K, esize, fp8);
 
-  CUtensorMap ta, to;
+  CUtensorMap ta, tw, to;
   {
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(lda * esize)};
@@ -945,6 +1084,22 @@ frt_status gemm_common(bool fp8, const void* a, int64_t lda, const float* a_scal
                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return FRT_ERR_CUDA;
+  }
+  if (pl.pair) {
+    // packed weight tiles as rows of 128 bytes (the tiles are stored in
+    // their shared-memory image, so no swizzle); one box = the 128 or 64
+    // channels of one k-block that a pair's CTA holds
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kKBytes),
+                                static_cast<cuuint64_t>(nb_total * kb_total * kTile)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kKBytes)};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kKBytes), static_cast<cuuint32_t>(pl.bn / 2)};
+    const cuuint32_t estr[2] = {1, 1};
+    if (encode(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(w_packed), dims, strides,
+               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return FRT_ERR_CUDA;
+  } else {
+    tw = ta;  // not read by the single-CTA kernels
   }
   {
     // output boxes, one per epilogue warp and chunk: {32 channels, 32 rows}
@@ -967,8 +1122,8 @@ frt_status gemm_common(bool fp8, const void* a, int64_t lda, const float* a_scal
   ga.M = static_cast<int>(M);
   ga.N = static_cast<int>(N);
   ga.act_cols = act == FRT_ACT_GELU_TANH ? static_cast<int>(act_cols) : 0;
-  ga.kb_total = static_cast<int>(ceil_div(K * esize, kKBytes));
-  ga.nb_total = static_cast<int>(ceil_div(N, kTile));
+  ga.kb_total = static_cast<int>(kb_total);
+  ga.nb_total = static_cast<int>(nb_total);
   ga.kb_per_split = pl.kb_per_split;
   ga.splits = pl.splits;
   ga.tiles_m = pl.tiles_m;
@@ -982,8 +1137,8 @@ frt_status gemm_common(bool fp8, const void* a, int64_t lda, const float* a_scal
   ga.tail_off = pl.tail_off;
   ga.dev_status = dev_status;
 
-  cudaError_t e = fp8 ? dispatch<true>(ta, to, ga, pl, as_cuda(stream))
-                      : dispatch<false>(ta, to, ga, pl, as_cuda(stream));
+  cudaError_t e = fp8 ? dispatch<true>(ta, tw, to, ga, pl, as_cuda(stream))
+                      : dispatch<false>(ta, tw, to, ga, pl, as_cuda(stream));
   if (e != cudaSuccess) {
     cudaGetLastError();
     return FRT_ERR_CUDA;
