@@ -476,5 +476,39 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
   }
 }
 
+// ---------------------------------------------------------------- global counters
+
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Adds 1 to a global counter, ordered after every write that happens before
+// it (cumulative release at GPU scope).
+__device__ __forceinline__ void counter_add_release(unsigned* p) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(p) : "memory");
+}
+
+// Waits until *ctr >= target (acquire).  Same time limit and abort protocol
+// as mbar_wait.
+__device__ __forceinline__ bool wait_counter(const unsigned* ctr, unsigned target,
+                                             volatile int* abort, int* status, int code) {
+  if (ld_acquire_gpu(ctr) >= target) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    __nanosleep(64);
+    if (ld_acquire_gpu(ctr) >= target) return true;
+    if ((it & 15u) == 0u) {
+      if (abort && *abort) return false;
+      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        if (abort) *abort = 1;
+        if (status) atomicCAS(status, 0, code);
+        return false;
+      }
+    }
+  }
+}
+
 }  // namespace dev
 }  // namespace frt

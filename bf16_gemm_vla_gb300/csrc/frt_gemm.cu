@@ -81,6 +81,9 @@ struct GemmArgs {
   int outbuf_off;      // shared-memory layout (bytes from the 1024-aligned base)
   int recv_off;
   int tail_off;        // per-channel scale/bias, then mbarriers
+  int split_global;    // split-K partials exchanged through the workspace (pairs)
+  float* ws_part;      // split_global: partial chunks, one slot per (tile, CTA, chunk, split)
+  unsigned* ws_flag;   // split_global: per (tile, CTA, owner split) arrival counters
   int* dev_status;
 };
 
@@ -196,10 +199,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x & 31;
   const bool split = p.splits > 1;
   const int S = p.splits;
-  // cluster layout: a pair's two CTAs along x, split-K ranks along z
+  // split-K partials meet in the workspace (global split; pairs only) or in
+  // the shared memory of one cluster (cluster split)
+  const bool gsplit = kPair && split && p.split_global;
+  const bool csplit = split && !gsplit;
+  // cluster layout: a pair's two CTAs along x, cluster-split ranks along z
   const uint32_t crank = (kPair || split) ? dev::cluster_ctarank() : 0u;
   const int px = kPair ? static_cast<int>(crank & 1u) : 0;  // CTA within the pair
-  const int rank = kPair ? static_cast<int>(crank >> 1) : static_cast<int>(crank);  // K split
+  const int rank = gsplit ? static_cast<int>(blockIdx.z)
+                          : (kPair ? static_cast<int>(crank >> 1) : static_cast<int>(crank));
   const bool leader = px == 0;  // issues the pair's MMAs
   const uint32_t lead_rank = crank & ~1u;
   // cluster rank of the CTA that holds K split j of this CTA's rows
@@ -230,7 +238,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     dev::mbar_init(recv_bar, 1);
     *abort_flag = 0;
     dev::fence_mbar_init();
-    if (split)  // bytes this CTA receives: its own chunks from every peer
+    if (csplit)  // bytes this CTA receives: its own chunks from every peer
       dev::mbar_arrive_expect_tx(recv_bar, static_cast<uint32_t>(S - 1) *
                                                static_cast<uint32_t>(own_c1 - own_c0) *
                                                chunk_bytes);
@@ -263,7 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // thread arrives now (its mbarriers are initialised); when the receive
   // buffers reuse the stage buffers, each thread arrives once this CTA's
   // MMAs can no longer read them.
-  if (split && !p.recv_in_stages) dev::cluster_arrive_relaxed();
+  if (csplit && !p.recv_in_stages) dev::cluster_arrive_relaxed();
 
   // this CTA's tiles: split -> one tile and a K range; else a strided list
   // (a pair walks its list together)
@@ -558,6 +566,71 @@ __global__ void __launch_bounds__(kThreads, 1)
           release_acc(b);
           finish32(v, 0, tm * kBN);
         }
+      } else if (gsplit) {
+        if constexpr (!kSwap) {
+          // ------------- split-K: exchange partial chunks through the workspace
+          // slot of (tile, CTA of the pair, chunk c, split j): 128 rows x 32
+          // columns, float4 granule q of row r at (q * 128 + r)
+          const int tile = first_tile;
+          auto slot = [&](int c, int j) -> float4* {
+            return reinterpret_cast<float4*>(p.ws_part) +
+                   (static_cast<size_t>((tile * 2 + px) * NC + c) * S + j) * (kTile * 8);
+          };
+          auto flag = [&](int o) { return p.ws_flag + (tile * 2 + px) * S + o; };
+          // 1. the chunks other splits own -> their slots
+          for (int c = 0; c < NC; ++c) {
+            if (c >= own_c0 && c < own_c1) continue;
+            float v[32];
+            dev::tmem_ld32(tacc + c * 32, v);
+            float4* dst = slot(c, rank);
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              __stcg(dst + q * kTile + row,
+                     make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]));
+          }
+          __threadfence();
+          dev::named_sync(1, 128);
+          if (et == 0) {
+            for (int o = 0; o < S; ++o)
+              if (o != rank && chunk_begin(o) < chunk_begin(o + 1)) dev::counter_add_release(flag(o));
+            // 2. wait (bounded) until the other S - 1 splits have written
+            //    this CTA's chunks, then return the counter to zero
+            if (own_c1 > own_c0) {
+              if (dev::wait_counter(flag(rank), static_cast<unsigned>(S - 1), abort_flag,
+                                    p.dev_status, dev::kTimeoutEpilogue))
+                *flag(rank) = 0u;
+              else
+                ok = false;
+            }
+          }
+          dev::named_sync(1, 128);
+          ok = !*abort_flag && ok;
+          // 3. own chunks: the S partials added in split order
+          for (int c = own_c0; c < own_c1; ++c) {
+            float acc[32];
+            dev::tmem_ld32(tacc + c * 32, acc);
+            float sum[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) sum[j] = 0.0f;
+            for (int r = 0; r < S; ++r) {
+              if (r == rank) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) sum[j] += acc[j];
+              } else {
+                const float4* src = slot(c, r);
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                  const float4 x = __ldcg(src + q * kTile + row);
+                  sum[4 * q] += x.x;
+                  sum[4 * q + 1] += x.y;
+                  sum[4 * q + 2] += x.z;
+                  sum[4 * q + 3] += x.w;
+                }
+              }
+            }
+            finish32(sum, c * 32, 0);
+          }
+        }
       } else {
         // ------------- split-K: exchange partial chunks inside the cluster
         const int owned = own_c1 - own_c0;
@@ -732,7 +805,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) dev::bulk_wait_all();  // stores complete before the grid ends
   }
 
-  if (split) {
+  if (csplit) {
     if (warp < 2) {  // the copy and MMA warps: both barrier phases
       if (p.recv_in_stages) dev::cluster_arrive();
       dev::cluster_wait();
@@ -786,6 +859,9 @@ struct Plan {
   int chunk_cols;
   int stages;
   bool recv_in_stages;
+  bool split_global;  // split-K through the workspace (CTA pairs)
+  size_t ws_bytes;    // workspace the plan uses (split_global), else 0
+  size_t ws_flag_bytes;
   int outbuf_off, recv_off, tail_off;
   int smem;
   dim3 grid;
@@ -797,7 +873,7 @@ bool layout(Plan& pl, int stage_bytes) {
   pl.outbuf_off = pipe;
   pl.recv_off = 0;
   int tail = pipe + kOutBytes;
-  if (pl.splits > 1) {
+  if (pl.splits > 1 && !pl.split_global) {
     const int nchunks = pl.bn / pl.chunk_cols;
     const int chunk = kTile * pl.chunk_cols * 4;
     const int owned_max = static_cast<int>(ceil_div(nchunks, pl.splits));
@@ -900,7 +976,7 @@ int cluster_capacity_for(const Plan& pl, int s, int smem) {
 bool place_buffers(Plan& pl, int stage_bytes, int want) {
   int best = 0;
   bool best_in_stages = false;
-  for (int mode = 0; mode < (pl.splits > 1 ? 2 : 1); ++mode) {
+  for (int mode = 0; mode < (pl.splits > 1 && !pl.split_global ? 2 : 1); ++mode) {
     pl.recv_in_stages = mode == 1;
     for (int st = kMaxStages; st >= 2; --st) {
       if (!pl.recv_in_stages && st > want) continue;
@@ -927,8 +1003,21 @@ bool place_buffers(Plan& pl, int stage_bytes, int want) {
 // kind and width, split-K factor, grid and pipeline depth.  The split is the
 // largest one that fits shared memory and keeps every cluster resident in
 // one wave.
-Plan make_plan(int64_t M, int64_t N, int64_t K, int esize, bool fp8) {
+// Workspace of a global split: the arrival counters, then one 16 KiB slot per
+// (tile, CTA of the pair, 32-column chunk, split).
+void global_split_bytes(Plan& pl) {
+  const int nchunks = pl.bn / pl.chunk_cols;
+  pl.ws_flag_bytes = static_cast<size_t>(ceil_div(
+                         static_cast<int64_t>(pl.num_tiles) * 2 * pl.splits * 4, 256)) * 256;
+  pl.ws_bytes = pl.ws_flag_bytes + static_cast<size_t>(pl.num_tiles) * 2 * nchunks * pl.splits *
+                                       static_cast<size_t>(kTile * pl.chunk_cols * 4);
+}
+
+Plan make_plan(int64_t M, int64_t N, int64_t K, int esize, bool fp8, size_t ws_avail) {
   Plan pl;
+  pl.split_global = false;
+  pl.ws_bytes = 0;
+  pl.ws_flag_bytes = 0;
   const int kb = static_cast<int>(ceil_div(K * esize, kKBytes));
   const int nb = static_cast<int>(ceil_div(N, kTile));
   const int sms = sm_count() > 0 ? sm_count() : 148;
@@ -960,16 +1049,35 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int esize, bool fp8) {
   const int w_rows = pl.swap ? kTile : (pl.pair ? pl.bn / 2 : pl.bn);
   const int stage_bytes = (act_rows + w_rows) * kKBytes;
 
-  int s_max = 1;
+  int s_max = 1, g_max = 1;
   if (pl.num_tiles * ctas_per_tile < sms) {
     s_max = sms / (pl.num_tiles * ctas_per_tile);
     const int nchunks = pl.bn / pl.chunk_cols;
-    if (s_max > kMaxSplits / ctas_per_tile) s_max = kMaxSplits / ctas_per_tile;
     if (s_max > nchunks) s_max = nchunks;
     if (s_max > kb) s_max = kb;
     if (s_max < 1) s_max = 1;
+    g_max = pl.pair ? s_max : 1;  // a global split is not bounded by the cluster size
+    if (s_max > kMaxSplits / ctas_per_tile) s_max = kMaxSplits / ctas_per_tile;
   }
-  for (int s = s_max; s >= 1; --s) {
+  // CTA pairs: split K through the workspace when the caller gave enough of
+  // it and every pair of the grid can be resident at once (the owners of
+  // each chunk wait for the other splits' partials)
+  for (int s = g_max; s >= 2; --s) {
+    pl.kb_per_split = static_cast<int>(ceil_div(kb, s));
+    pl.splits = static_cast<int>(ceil_div(kb, pl.kb_per_split));
+    if (pl.splits < 2) break;
+    pl.split_global = true;
+    global_split_bytes(pl);
+    if (pl.ws_bytes <= ws_avail && place_buffers(pl, stage_bytes, kMaxStages)) {
+      const int smem = pl.smem < kPairMinSmem ? kPairMinSmem : pl.smem;
+      const int capacity = fp8 ? cluster_capacity_for<true>(pl, 1, smem)
+                               : cluster_capacity_for<false>(pl, 1, smem);
+      if (capacity >= pl.num_tiles * pl.splits) break;
+    }
+    pl.split_global = false;
+    pl.ws_bytes = pl.ws_flag_bytes = 0;
+  }
+  for (int s = pl.split_global ? 0 : s_max; s >= 1; --s) {
     pl.kb_per_split = static_cast<int>(ceil_div(kb, s));
     pl.splits = static_cast<int>(ceil_div(kb, pl.kb_per_split));
     // pipeline depth: small M takes just the CTA's k-blocks (a small
@@ -992,7 +1100,7 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int esize, bool fp8) {
   // shared memory no other GEMM CTA (each takes over 40 KiB) is resident
   // beside it, while the small CTAs of other kernels still are
   if (pl.pair && pl.smem < kPairMinSmem) pl.smem = kPairMinSmem;
-  if (pl.splits > 1) {
+  if (pl.split_global || pl.splits > 1) {
     pl.grid = dim3(static_cast<unsigned>(pl.num_tiles * ctas_per_tile), 1,
                    static_cast<unsigned>(pl.splits));
   } else {
@@ -1021,7 +1129,7 @@ cudaError_t launch_one(const CUtensorMap& ta, const CUtensorMap& tw, const CUten
   attr[1].id = cudaLaunchAttributeClusterDimension;
   attr[1].val.clusterDim.x = kPair ? 2 : 1;
   attr[1].val.clusterDim.y = 1;
-  attr[1].val.clusterDim.z = pl.splits;
+  attr[1].val.clusterDim.z = pl.split_global ? 1 : pl.splits;
   cfg.attrs = attr;
   cfg.numAttrs = (kPair || pl.splits > 1) ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, kern, ta, tw, to, a);
@@ -1046,7 +1154,8 @@ cudaError_t dispatch(const CUtensorMap& ta, const CUtensorMap& tw, const CUtenso
 frt_status gemm_common(bool fp8, const void* a, int64_t lda, const float* a_scale,
                        const void* w_packed, const float* w_scale, const float* bias, int64_t M,
                        int64_t N, int64_t K, frt_act act, int64_t act_cols, void* out,
-                       int64_t ldo, int* dev_status, frt_stream_t stream) {
+                       int64_t ldo, void* workspace, size_t workspace_bytes, int* dev_status,
+                       frt_stream_t stream) {
   const int esize = fp8 ? 1 : 2;
   if (!a || !w_packed || !out) return FRT_ERR_INVALID_ARG;
   if (fp8 && (!a_scale || !w_scale)) return FRT_ERR_INVALID_ARG;
@@ -1070,7 +1179,9 @@ frt_status gemm_common(bool fp8, const void* a, int64_t lda, const float* a_scal
 
   auto encode = tensor_map_encoder();
   if (!encode) return FRT_ERR_CUDA;
-  const Plan pl = make_plan(M, N, K, esize, fp8);
+  // a workspace that is missing or misaligned is not used
+  const size_t ws_avail = (workspace && aligned(workspace, 256)) ? workspace_bytes : 0;
+  const Plan pl = make_plan(M, N, K, esize, fp8, ws_avail);
 
   CUtensorMap ta, tw, to;
   {
@@ -1135,6 +1246,11 @@ frt_status gemm_common(bool fp8, const void* a, int64_t lda, const float* a_scal
   ga.outbuf_off = pl.outbuf_off;
   ga.recv_off = pl.recv_off;
   ga.tail_off = pl.tail_off;
+  ga.split_global = pl.split_global ? 1 : 0;
+  ga.ws_flag = pl.split_global ? static_cast<unsigned*>(workspace) : nullptr;
+  ga.ws_part = pl.split_global
+                   ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + pl.ws_flag_bytes)
+                   : nullptr;
   ga.dev_status = dev_status;
 
   cudaError_t e = fp8 ? dispatch<true>(ta, tw, to, ga, pl, as_cuda(stream))
@@ -1149,23 +1265,30 @@ frt_status gemm_common(bool fp8, const void* a, int64_t lda, const float* a_scal
 }  // namespace
 }  // namespace frt
 
-extern "C" size_t frt_gemm_workspace_bytes(int64_t, int64_t, int64_t, frt_dtype) { return 0; }
+extern "C" size_t frt_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, frt_dtype a_dtype) {
+  // only CTA-pair plans (M > 128) split K through the workspace
+  if (M <= 128 || N < 1 || K < 1) return 0;
+  if (a_dtype != FRT_E4M3_OCP && a_dtype != FRT_BF16) return 0;
+  const bool fp8 = a_dtype == FRT_E4M3_OCP;
+  const frt::Plan pl = frt::make_plan(M, N, K, fp8 ? 1 : 2, fp8, static_cast<size_t>(-1));
+  return pl.ws_bytes;
+}
 
 extern "C" frt_status frt_gemm_fp8(const uint8_t* a_q, int64_t lda, const float* a_scale,
                                    const void* w_packed, const float* w_scale, const float* bias,
                                    int64_t M, int64_t N, int64_t K, frt_act act, int64_t act_cols,
-                                   void* out, int64_t ldo, void* /*workspace*/,
-                                   size_t /*workspace_bytes*/, int* dev_status,
+                                   void* out, int64_t ldo, void* workspace,
+                                   size_t workspace_bytes, int* dev_status,
                                    frt_stream_t stream) {
   return frt::gemm_common(true, a_q, lda, a_scale, w_packed, w_scale, bias, M, N, K, act,
-                          act_cols, out, ldo, dev_status, stream);
+                          act_cols, out, ldo, workspace, workspace_bytes, dev_status, stream);
 }
 
 extern "C" frt_status frt_gemm_bf16(const void* a, int64_t lda, const void* w_packed,
                                     const float* w_scale, const float* bias, int64_t M, int64_t N,
                                     int64_t K, frt_act act, int64_t act_cols, void* out,
-                                    int64_t ldo, void* /*workspace*/, size_t /*workspace_bytes*/,
+                                    int64_t ldo, void* workspace, size_t workspace_bytes,
                                     int* dev_status, frt_stream_t stream) {
   return frt::gemm_common(false, a, lda, nullptr, w_packed, w_scale, bias, M, N, K, act, act_cols,
-                          out, ldo, dev_status, stream);
+                          out, ldo, workspace, workspace_bytes, dev_status, stream);
 }

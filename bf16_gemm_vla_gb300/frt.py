@@ -162,6 +162,46 @@ def check_device_status(device=None):
         raise FrtError("device wait (code 0x%x)" % code, 6)
 
 
+_GEMM_DTYPE = {"e4m3": _lib.FRT_E4M3_OCP, "bf16": _lib.FRT_BF16}
+_GEMM_WS = {}
+_GEMM_WS_RETIRED = []
+
+
+def frt_gemm_workspace_bytes(M, N, K, kind="e4m3"):
+    """Bytes of GEMM workspace the plan of this shape uses on the current
+    device (0: none).  A workspace must be zero-filled before its first use;
+    the GEMM leaves it so."""
+    return lib().frt_gemm_workspace_bytes(M, N, K, _GEMM_DTYPE[kind])
+
+
+def gemm_workspace(M, N, K, kind="e4m3", device=None):
+    """A zero-filled workspace for one layer's GEMM (None if it needs none)."""
+    nb = frt_gemm_workspace_bytes(M, N, K, kind)
+    if nb == 0:
+        return None
+    return torch.zeros((nb,), dtype=torch.uint8, device=device)
+
+
+def _gemm_ws(workspace, M, N, K, kind, device):
+    """(pointer, bytes) of the workspace to pass: the caller's; none for
+    workspace=False; else a per-device shared one (calls that use it must be
+    ordered on one stream), grown on demand."""
+    if workspace is False:
+        return None, 0
+    if workspace is not None:
+        return workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    nb = frt_gemm_workspace_bytes(M, N, K, kind)
+    if nb == 0:
+        return None, 0
+    ws = _GEMM_WS.get(device)
+    if ws is None or ws.numel() < nb:
+        if ws is not None:
+            _GEMM_WS_RETIRED.append(ws)  # may still be in use by queued work
+        ws = torch.zeros((nb,), dtype=torch.uint8, device=device)
+        _GEMM_WS[device] = ws
+    return ws.data_ptr(), ws.numel()
+
+
 def _gemm_out(M, N, out, device):
     if out is None:
         out = torch.empty((M, N), dtype=torch.bfloat16, device=device)
@@ -172,27 +212,33 @@ def _gemm_out(M, N, out, device):
 
 
 def frt_gemm_fp8(a_q, a_scale, w_packed, w_scale, N, bias=None, act_cols=0, out=None,
-                 stream=None):
+                 stream=None, workspace=None):
     """out = bf16(act(a_scale * w_scale[n] * (A_q . W) + bias[n])), GELU on
-    the first act_cols columns.  a_q: [M x K] OCP E4M3 bytes."""
+    the first act_cols columns.  a_q: [M x K] OCP E4M3 bytes.  workspace: a
+    zero-filled uint8 tensor of frt_gemm_workspace_bytes() bytes, False for
+    none, or None for the shared per-device one."""
     M, K, lda = _rows_view(a_q, "a_q")
     out, ldo = _gemm_out(M, N, out, a_q.device)
     act = _lib.FRT_ACT_GELU_TANH if act_cols else _lib.FRT_ACT_NONE
+    wp, wb = _gemm_ws(workspace, M, N, K, "e4m3", a_q.device)
     _check("frt_gemm_fp8",
            lib().frt_gemm_fp8(a_q.data_ptr(), lda, _ptr(a_scale), w_packed.data_ptr(),
                               _ptr(w_scale), _ptr(bias), M, N, K, act, act_cols, out.data_ptr(),
-                              ldo, None, 0, device_status(a_q.device).data_ptr(),
+                              ldo, wp, wb, device_status(a_q.device).data_ptr(),
                               _stream(stream)))
     return out
 
 
-def frt_gemm_bf16(a, w_packed, N, w_scale=None, bias=None, act_cols=0, out=None, stream=None):
-    """out = bf16(act(w_scale[n] * (A . W) + bias[n])).  a: [M x K] bf16."""
+def frt_gemm_bf16(a, w_packed, N, w_scale=None, bias=None, act_cols=0, out=None, stream=None,
+                  workspace=None):
+    """out = bf16(act(w_scale[n] * (A . W) + bias[n])).  a: [M x K] bf16.
+    workspace as for frt_gemm_fp8."""
     M, K, lda = _rows_view(a, "a")
     out, ldo = _gemm_out(M, N, out, a.device)
     act = _lib.FRT_ACT_GELU_TANH if act_cols else _lib.FRT_ACT_NONE
+    wp, wb = _gemm_ws(workspace, M, N, K, "bf16", a.device)
     _check("frt_gemm_bf16",
            lib().frt_gemm_bf16(a.data_ptr(), lda, w_packed.data_ptr(), _ptr(w_scale), _ptr(bias),
-                               M, N, K, act, act_cols, out.data_ptr(), ldo, None, 0,
+                               M, N, K, act, act_cols, out.data_ptr(), ldo, wp, wb,
                                device_status(a.device).data_ptr(), _stream(stream)))
     return out

@@ -75,6 +75,9 @@ class Linear:
             self.a_scale = torch.empty((1,), dtype=torch.float32, device=dev)
             nb = frt.frt_quantize_workspace_bytes(M, weight.K, frt.PER_TENSOR)
             self.ws = torch.empty((max(nb, 4) // 4,), dtype=torch.float32, device=dev)
+        # the GEMM's own (zero-filled) workspace, or False if it needs none
+        gws = frt.gemm_workspace(M, weight.N, weight.K, weight.kind, dev)
+        self.gws = False if gws is None else gws
 
     def __call__(self, x, stream=None):
         w = self.w
@@ -82,6 +85,8 @@ class Linear:
             frt.frt_quantize_e4m3(x, frt.PER_TENSOR, frt.OCP, q=self.q, scale=self.a_scale,
                                   workspace=self.ws, stream=stream)
             return frt.frt_gemm_fp8(self.q, self.a_scale, w.packed, w.w_scale, w.N, bias=w.bias,
-                                    act_cols=self.act_cols, out=self.out, stream=stream)
+                                    act_cols=self.act_cols, out=self.out, stream=stream,
+                                    workspace=self.gws)
         return frt.frt_gemm_bf16(x, w.packed, w.N, w_scale=w.w_scale, bias=w.bias,
-                                 act_cols=self.act_cols, out=self.out, stream=stream)
+                                 act_cols=self.act_cols, out=self.out, stream=stream,
+                                 workspace=self.gws)

@@ -49,7 +49,7 @@ def main(argv=None):
             if a.with_quantize:
                 return lin(x)
             return frt.frt_gemm_fp8(lin.q, lin.a_scale, pw.packed, pw.w_scale, pw.N, bias=b,
-                                    act_cols=a.act_cols, out=lin.out)
+                                    act_cols=a.act_cols, out=lin.out, workspace=lin.gws)
         return lin(x)
 
     once()

@@ -213,10 +213,21 @@ frt_status frt_pack_weights(const void* w, frt_dtype w_dtype, int64_t K, int64_t
  * out       : bf16 [M x N], row stride ldo; 16-byte aligned, ldo a multiple of 8.
  * act_cols  : number of leading output columns the activation applies to
  *             (0 <= act_cols <= N; a merged gate/up GEMM passes N/2).
- * workspace : reserved; frt_gemm_workspace_bytes() returns 0 and the
- *             pointer may be NULL.  (Split-K partial sums are reduced across
- *             the CTAs of a thread-block cluster in shared memory, in a fixed
- *             order, so results are deterministic.)
+ * workspace : optional device scratch for split-K, 256-byte aligned, of at
+ *             least frt_gemm_workspace_bytes() bytes (that function returns
+ *             0 when the shape's plan has no use for one; a_dtype is
+ *             FRT_E4M3_OCP for frt_gemm_fp8, FRT_BF16 for frt_gemm_bf16).
+ *             It must be zero-filled before its first use.  Every call
+ *             returns the arrival counters it holds to zero, so it is reused
+ *             as it is (the rest of it holds dead partial sums), unless
+ *             dev_status reports a timeout: then the caller zero-fills it
+ *             again.  Calls
+ *             that share a workspace must be ordered on one stream.  With
+ *             NULL, a misaligned pointer or fewer bytes the GEMM takes a plan
+ *             that needs none.  Either way split-K partial sums are added in
+ *             a fixed order (across the CTAs of a thread-block cluster in
+ *             shared memory, or through the workspace), so a given shape and
+ *             workspace choice give bit-identical results run to run.
  * dev_status: optional device int.  Every wait inside the kernels is
  *             bounded (about one second); if one expires the kernel writes a
  *             nonzero code there (the first writer wins), abandons its tile

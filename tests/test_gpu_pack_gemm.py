@@ -233,3 +233,60 @@ def test_sweep_shapes(M):
     lay = synth.sweep_gemm(M, seed=M)
     fp8_layer(lay)
     bf16_layer(lay)
+
+
+# ---------------------------------------------------------------- split-K through the workspace
+
+@pytest.mark.parametrize("M,K,N", [(768, 16384, 2048), (300, 16384, 256), (520, 8192, 384)])
+def test_split_k_workspace_and_cluster_paths(M, K, N):
+    # large-M shapes whose K is split: with a workspace the partial sums meet
+    # in global memory, without one inside a cluster; both match the oracle,
+    # each is bit-identical from call to call, and the workspace's counters
+    # are back at zero after every call (a second input through the same
+    # workspace is not mixed with the first)
+    nb = frt.frt_gemm_workspace_bytes(M, N, K, "e4m3")
+    assert nb > 0
+    ws = torch.zeros((nb,), dtype=torch.uint8, device="cuda")
+    for seed in (K + N, K + N + 1):
+        lay = rand_layer(M, K, N, seed=seed)
+        a_dev = bf16_dev(lay["a_bf16"])
+        qa, sa = frt.frt_quantize_e4m3(a_dev, frt.PER_TENSOR, frt.OCP)
+        pw = layers.prepare_fp8(torch.from_numpy(lay["w_f32"]).cuda(),
+                                torch.from_numpy(lay["bias"]).cuda())
+        outs = {}
+        # a workspace too small for any global split: the cluster path
+        tiny = torch.zeros((256,), dtype=torch.uint8, device="cuda")
+        for name, w in (("workspace", ws), ("cluster", False), ("too_small", tiny)):
+            o1 = frt.frt_gemm_fp8(qa, sa, pw.packed, pw.w_scale, N, bias=pw.bias, workspace=w)
+            o2 = frt.frt_gemm_fp8(qa, sa, pw.packed, pw.w_scale, N, bias=pw.bias, workspace=w)
+            frt.check_device_status()
+            assert torch.equal(o1, o2), name
+            outs[name] = o1
+        assert int(ws[:256].sum()) == 0
+        assert torch.equal(outs["too_small"], outs["cluster"])
+        qa_o, sa_o = quantize.quantize_e4m3(synth.bf16_bits_as_f32(lay["a_bf16"]),
+                                            quantize.PER_TENSOR, e4m3.OCP)
+        qw_o, sw_o = quantize.quantize_e4m3(lay["w_f32"], quantize.PER_COL, e4m3.OCP)
+        y, sumabs = gemm.gemm_fp8(qa_o, e4m3.OCP, sa_o, qw_o, e4m3.OCP, sw_o, lay["bias"], 0)
+        for name, o in outs.items():
+            assert_gemm_close(o, y, sumabs, "%s M=%d K=%d N=%d" % (name, M, K, N))
+
+
+def test_split_k_workspace_bf16():
+    M, K, N = 768, 16384, 2048
+    lay = rand_layer(M, K, N, seed=5)
+    nb = frt.frt_gemm_workspace_bytes(M, N, K, "bf16")
+    assert nb > 0
+    ws = torch.zeros((nb,), dtype=torch.uint8, device="cuda")
+    a_dev = bf16_dev(lay["a_bf16"])
+    wp = frt.frt_pack_weights(torch.from_numpy(lay["w_f32"]).cuda(), "bf16")
+    b_dev = torch.from_numpy(lay["bias"]).cuda()
+    torch.cuda.synchronize()
+    o1 = frt.frt_gemm_bf16(a_dev, wp, N, bias=b_dev, workspace=ws)
+    o2 = frt.frt_gemm_bf16(a_dev, wp, N, bias=b_dev, workspace=ws)
+    frt.check_device_status()
+    assert torch.equal(o1, o2)
+    assert int(ws[:256].sum()) == 0
+    y, sumabs = gemm.gemm_bf16(synth.bf16_bits_as_f32(lay["a_bf16"]),
+                               obf16.round_to_bf16(lay["w_f32"]), None, lay["bias"], 0)
+    assert_gemm_close(o1, y, sumabs, "bf16 workspace split")
