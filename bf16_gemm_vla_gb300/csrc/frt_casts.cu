@@ -7,6 +7,7 @@
 // DeepSeek-V4-Flash on AMD MI300X", "The FP8 dialect problem").
 #include <cuda_bf16.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "frt_device.cuh"
@@ -362,6 +363,209 @@ __global__ void __launch_bounds__(kQThreads) encode_tensor_kernel(
   if (!early) dev::grid_launch_dependents();
 }
 
+// Per-tensor quantize in one grid, with the tensor resident on chip.
+//
+// Every CTA (all resident at once, at most one per SM) holds its part of x
+// on chip -- in registers for tensors up to kRegCapacity 16-byte vectors,
+// else in shared memory, bulk-copied as contiguous chunks -- and takes the
+// max |x| of it as it arrives.  The CTAs then meet at a grid barrier in the
+// workspace header, where the last to arrive turns the maximum into
+// s = amax / max (1 if amax is 0); finally every CTA encodes its part from
+// chip.  x is read from memory once.
+//
+// The barrier is a sense-reversing pair of counters: each CTA reads the
+// generation (after the previous grid has completed), folds its maximum into
+// the header's amax word (an unsigned max of the non-negative fp32 bits),
+// then arrives; the last arrival reads the amax, resets it and the arrival
+// count, publishes s and advances the generation, which releases the
+// others.  Waits are bounded; a CTA that gives up records a code in the
+// header's status word and uses s = NaN, so the result is visibly invalid.
+constexpr int kResThreads = 512;
+constexpr int kResChunk = 16384;    // bytes per bulk copy
+constexpr int kResMaxChunks = 13;   // at most 208 KiB of a tensor per CTA
+constexpr int kResSmem = kResChunk * kResMaxChunks;
+constexpr int kRegVecs = 4;         // register path: 16-byte vectors per thread
+constexpr int kHeaderFloats = 64;   // workspace header: 256 bytes
+// header words: [0] arrivals, [1] generation, [2] scale bits, [3] status, [4] amax bits
+
+__device__ __forceinline__ unsigned atom_add_acq_rel_gpu(unsigned* p, unsigned v) {
+  unsigned old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v)
+               : "memory");
+  return old;
+}
+
+template <typename T>
+__device__ __forceinline__ int unpack16(const uint4& w, float (&f)[8]) {
+  if constexpr (sizeof(T) == 2) {
+    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      f[2 * k] = __uint_as_float(ws[k] << 16);
+      f[2 * k + 1] = __uint_as_float(ws[k] & 0xFFFF0000u);
+    }
+    return 8;
+  } else {
+    f[0] = __uint_as_float(w.x); f[1] = __uint_as_float(w.y);
+    f[2] = __uint_as_float(w.z); f[3] = __uint_as_float(w.w);
+    return 4;
+  }
+}
+
+// E4M3 bytes of one 16-byte vector of x at q + e (8 or 4 elements).
+template <typename T, bool kFnuz>
+__device__ __forceinline__ void encode16(const uint4& w, float sc, float r, bool fast_ok,
+                                         uint8_t* dst) {
+  float f[8];
+  unpack16<T>(w, f);
+  uint32_t lo = 0, hi = 0;
+  if constexpr (kFnuz) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) lo |= quantize_one<true>(f[k], sc, r, fast_ok) << (8 * k);
+    if constexpr (sizeof(T) == 2) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) hi |= quantize_one<true>(f[4 + k], sc, r, fast_ok) << (8 * k);
+    }
+  } else {
+    lo = canonical_nan_x4(quantize_pair_ocp(f[0], f[1], sc, r, fast_ok) |
+                          (quantize_pair_ocp(f[2], f[3], sc, r, fast_ok) << 16));
+    if constexpr (sizeof(T) == 2)
+      hi = canonical_nan_x4(quantize_pair_ocp(f[4], f[5], sc, r, fast_ok) |
+                            (quantize_pair_ocp(f[6], f[7], sc, r, fast_ok) << 16));
+  }
+  if constexpr (sizeof(T) == 2)
+    *reinterpret_cast<uint2*>(dst) = make_uint2(lo, hi);
+  else
+    *reinterpret_cast<uint32_t*>(dst) = lo;
+}
+
+template <typename T>
+__device__ __forceinline__ float max16(const uint4& w, float m) {
+  float f[8];
+  const int ne = unpack16<T>(w, f);
+#pragma unroll
+  for (int k = 0; k < 8; ++k)
+    if (k < ne) m = fmaxf(m, fabsf(f[k]));
+  return m;
+}
+
+// The grid barrier above.  m: this CTA's max |x| (valid in thread 0); g0:
+// the generation read by thread 0 after the dependency wait.  Returns s (or
+// NaN if this CTA gave up) in every thread.
+template <bool kFnuz>
+__device__ __forceinline__ float grid_scale(float m, unsigned g0, unsigned* hdr, bool failed) {
+  __shared__ float s_sh;
+  __shared__ int fail_sh;
+  if (threadIdx.x == 0) {
+    fail_sh = failed;
+    atomicMax(hdr + 4, __float_as_uint(m));
+    if (atom_add_acq_rel_gpu(hdr, 1u) == gridDim.x - 1) {
+      const float a = __uint_as_float(dev::ld_acquire_gpu(hdr + 4));
+      const float sc = a == 0.0f ? 1.0f : __fdiv_rn(a, kFnuz ? 240.0f : 448.0f);
+      hdr[2] = __float_as_uint(sc);
+      hdr[4] = 0u;
+      hdr[0] = 0u;
+      dev::counter_add_release(hdr + 1);
+      s_sh = sc;
+    } else if (dev::wait_counter_change(hdr + 1, g0)) {
+      s_sh = __uint_as_float(__ldcg(hdr + 2));
+    } else {
+      fail_sh = 1;
+    }
+    if (fail_sh) {
+      s_sh = __uint_as_float(0x7FC00000u);
+      atomicCAS(hdr + 3, 0u, 0x201u);
+    }
+  }
+  __syncthreads();
+  return s_sh;
+}
+
+// Register path: thread t of CTA b holds vectors t + 512 (b + G j), j < kRegVecs.
+template <typename T, bool kFnuz>
+__global__ void __launch_bounds__(kResThreads) quantize_regs_kernel(
+    const T* __restrict__ x, int64_t n_vec, uint8_t* __restrict__ q, float* __restrict__ scale_out,
+    unsigned* __restrict__ hdr) {
+  constexpr int VEC = 16 / sizeof(T);
+  __shared__ float red[32];
+  dev::grid_dependency_wait();  // x may come from the previous grid
+  const unsigned g0 = threadIdx.x == 0 ? dev::ld_acquire_gpu(hdr + 1) : 0u;
+  const uint4* xv = reinterpret_cast<const uint4*>(x);
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * kResThreads;
+  const int64_t v0 = static_cast<int64_t>(blockIdx.x) * kResThreads + threadIdx.x;
+  uint4 w[kRegVecs];
+#pragma unroll
+  for (int j = 0; j < kRegVecs; ++j)
+    w[j] = v0 + j * stride < n_vec ? __ldcs(xv + v0 + j * stride) : make_uint4(0, 0, 0, 0);
+  float m = 0.0f;
+#pragma unroll
+  for (int j = 0; j < kRegVecs; ++j) m = max16<T>(w[j], m);
+  m = block_max(m, red);
+  const float sc = grid_scale<kFnuz>(m, g0, hdr, false);
+  dev::grid_launch_dependents();  // every CTA is past the barrier
+  if (blockIdx.x == 0 && threadIdx.x == 0 && scale_out) *scale_out = sc;
+  const float r = __frcp_rn(sc);
+  const bool fast_ok = recip_is_normal(sc, r);
+#pragma unroll
+  for (int j = 0; j < kRegVecs; ++j)
+    if (v0 + j * stride < n_vec) encode16<T, kFnuz>(w[j], sc, r, fast_ok, q + (v0 + j * stride) * VEC);
+}
+
+// Shared-memory path: CTA b holds the contiguous elements [b per_cta, +per_cta).
+template <typename T, bool kFnuz>
+__global__ void __launch_bounds__(kResThreads, 1) quantize_resident_kernel(
+    const T* __restrict__ x, int64_t n, int64_t per_cta, uint8_t* __restrict__ q,
+    float* __restrict__ scale_out, unsigned* __restrict__ hdr) {
+  constexpr int VEC = 16 / sizeof(T);
+  extern __shared__ __align__(128) uint8_t res[];
+  __shared__ uint64_t bars[kResMaxChunks];
+  __shared__ float red[32];
+  const int tid = threadIdx.x;
+  const int64_t e0 = static_cast<int64_t>(blockIdx.x) * per_cta;
+  const int64_t e1 = e0 + per_cta < n ? e0 + per_cta : n;
+  const uint32_t bytes = static_cast<uint32_t>((e1 > e0 ? e1 - e0 : 0) * sizeof(T));
+  const int nchunks = static_cast<int>((bytes + kResChunk - 1) / kResChunk);
+  const uint32_t bar0 = dev::smem_u32(bars);
+  if (tid == 0) {
+    for (int i = 0; i < nchunks; ++i) dev::mbar_init(bar0 + 8 * i, 1);
+    dev::fence_mbar_init();
+  }
+  __syncthreads();
+  dev::grid_dependency_wait();  // x may come from the previous grid
+  unsigned g0 = 0;
+  if (tid == 0) {
+    g0 = dev::ld_acquire_gpu(hdr + 1);
+    const uint64_t pol = dev::policy_evict_first();
+    const uint8_t* src = reinterpret_cast<const uint8_t*>(x + e0);
+    for (int i = 0; i < nchunks; ++i) {
+      const uint32_t sz = bytes - i * kResChunk < kResChunk ? bytes - i * kResChunk : kResChunk;
+      dev::mbar_arrive_expect_tx(bar0 + 8 * i, sz);
+      dev::bulk_load(dev::smem_u32(res + i * kResChunk), src + i * kResChunk, sz, bar0 + 8 * i,
+                     pol);
+    }
+  }
+  // max |x| of the slice, chunk by chunk as the copies land (NaN is ignored
+  // by fmaxf)
+  float m = 0.0f;
+  bool ok = true;
+  for (int i = 0; i < nchunks; ++i) {
+    ok = dev::mbar_wait(bar0 + 8 * i, 0, nullptr, nullptr, 0) && ok;
+    const uint32_t sz = bytes - i * kResChunk < kResChunk ? bytes - i * kResChunk : kResChunk;
+    for (uint32_t v = tid; v < sz / 16; v += kResThreads)
+      m = max16<T>(*reinterpret_cast<const uint4*>(res + i * kResChunk + v * 16), m);
+  }
+  m = block_max(m, red);
+  const bool failed = __syncthreads_or(!ok);
+  const float sc = grid_scale<kFnuz>(m, g0, hdr, failed);
+  dev::grid_launch_dependents();  // every CTA is past the barrier
+  if (blockIdx.x == 0 && tid == 0 && scale_out) *scale_out = sc;
+  const float r = __frcp_rn(sc);
+  const bool fast_ok = recip_is_normal(sc, r);
+  for (uint32_t v = tid; v < bytes / 16; v += kResThreads)
+    encode16<T, kFnuz>(*reinterpret_cast<const uint4*>(res + v * 16), sc, r, fast_ok,
+                       q + e0 + static_cast<int64_t>(v) * VEC);
+}
+
 // Per-column pass 1: block (bx, by) covers columns [bx*256, +256) and rows
 // [by*kColRowsPerBlock, +kColRowsPerBlock); partial[by * cols + c] = max |x|.
 template <typename T>
@@ -418,12 +622,86 @@ int tensor_grid(int64_t total_vecs, int per_sm, int limit) {
   return static_cast<int>(g < 1 ? 1 : g);
 }
 
+// Sets the resident kernel's dynamic shared memory limit once per device.
+template <typename T, bool kFnuz>
+bool resident_ready() {
+  static std::mutex mu;
+  static bool set[64] = {false};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!set[dev]) {
+    if (cudaFuncSetAttribute(quantize_resident_kernel<T, kFnuz>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kResSmem) != cudaSuccess) {
+      cudaGetLastError();
+      return false;
+    }
+    set[dev] = true;
+  }
+  return true;
+}
+
 template <typename T, bool kFnuz>
 frt_status quantize_typed(const T* x, int64_t rows, int64_t cols, int64_t ldx, frt_scale_mode mode,
-                          const float* static_scale, uint8_t* q, float* scale, float* ws,
+                          const float* static_scale, uint8_t* q, float* scale, float* ws_all,
                           cudaStream_t st) {
+  // the workspace starts with the header of the one-grid path; partials follow
+  unsigned* hdr = reinterpret_cast<unsigned*>(ws_all);
+  float* ws = ws_all ? ws_all + kHeaderFloats : nullptr;
   if (mode == FRT_SCALE_PER_TENSOR) {
     const bool vec = aligned(x, 16) && aligned(q, 8) && cols % 8 == 0 && ldx % 8 == 0;
+    const int64_t n = rows * cols;
+    const int sms = sm_count() > 0 ? sm_count() : 148;
+    const int64_t n_vec16 = n * static_cast<int64_t>(sizeof(T)) / 16;
+    if (!static_scale && vec && ldx == cols && aligned(ws_all, 16) &&
+        n_vec16 <= static_cast<int64_t>(sms) * kResThreads * kRegVecs) {
+      // one grid, the tensor in registers: at most one CTA per SM
+      const int grid = static_cast<int>(
+          std::min<int64_t>(sms, ceil_div(n_vec16, static_cast<int64_t>(kResThreads))));
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(grid);
+      cfg.blockDim = dim3(kResThreads);
+      cfg.stream = st;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+      attr[0].val.programmaticStreamSerializationAllowed = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      if (cudaLaunchKernelEx(&cfg, quantize_regs_kernel<T, kFnuz>, x, n_vec16, q, scale, hdr) !=
+          cudaSuccess) {
+        cudaGetLastError();
+        return FRT_ERR_CUDA;
+      }
+      return launch_status();
+    }
+    if (!static_scale && vec && ldx == cols && aligned(ws_all, 16) &&
+        n * static_cast<int64_t>(sizeof(T)) <= static_cast<int64_t>(sms) * kResSmem &&
+        resident_ready<T, kFnuz>()) {
+      // one grid, the tensor resident in shared memory: slices of a multiple
+      // of 64 elements, at most one CTA per SM
+      int64_t per = ceil_div(n, static_cast<int64_t>(sms));
+      per = ceil_div(per, static_cast<int64_t>(64)) * 64;
+      const int grid = static_cast<int>(ceil_div(n, per));
+      const size_t smem = static_cast<size_t>(
+          ceil_div(per * static_cast<int64_t>(sizeof(T)), static_cast<int64_t>(kResChunk)) *
+          kResChunk);
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(grid);
+      cfg.blockDim = dim3(kResThreads);
+      cfg.dynamicSmemBytes = smem;
+      cfg.stream = st;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+      attr[0].val.programmaticStreamSerializationAllowed = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      if (cudaLaunchKernelEx(&cfg, quantize_resident_kernel<T, kFnuz>, x, n, per, q, scale,
+                             hdr) != cudaSuccess) {
+        cudaGetLastError();
+        return FRT_ERR_CUDA;
+      }
+      return launch_status();
+    }
     const int64_t total = rows * (vec ? cols / 8 : cols);
     const int grid = tensor_grid(total, 6, kMaxPartials);  // amax: one partial per block
     const int egrid = tensor_grid(total, 8, 1 << 20);
@@ -475,9 +753,11 @@ frt_status quantize_typed(const T* x, int64_t rows, int64_t cols, int64_t ldx, f
 
 extern "C" size_t frt_quantize_workspace_bytes(int64_t rows, int64_t cols, frt_scale_mode mode) {
   if (rows < 0 || cols < 0) return 0;
+  const size_t header = static_cast<size_t>(frt::kHeaderFloats) * sizeof(float);
   if (mode == FRT_SCALE_PER_COL)
-    return static_cast<size_t>(frt::ceil_div(rows, frt::kColRowsPerBlock) * cols) * sizeof(float);
-  return static_cast<size_t>(frt::kMaxPartials) * sizeof(float);
+    return header +
+           static_cast<size_t>(frt::ceil_div(rows, frt::kColRowsPerBlock) * cols) * sizeof(float);
+  return header + static_cast<size_t>(frt::kMaxPartials) * sizeof(float);
 }
 
 extern "C" frt_status frt_quantize_e4m3(const void* x, frt_dtype x_dtype, int64_t rows,
@@ -550,16 +830,17 @@ extern "C" frt_status frt_fnuz_to_ocp(const uint8_t* in, uint8_t* out, size_t n,
 // forbids allocator calls once it is running, a plugin that only receives
 // raw device pointers from a host application, or code that records a CUDA
 // graph in a mode where allocation would break the capture.  For them,
-// frt_quantize_e4m3_noalloc keeps its scratch (the amax partials) in the
-// fixed array below instead of a caller-provided workspace.  Every GPU that
-// loads the library holds the array until the process exits.
+// frt_quantize_e4m3_noalloc keeps its workspace (the 256-byte header of the
+// one-grid path, zero from the moment the library loads, then the amax
+// partials) in the fixed array below instead of a caller-provided one.
+// Every GPU that loads the library holds the array until the process exits.
 
 namespace frt {
 namespace {
 
-constexpr int64_t kNoAllocScratchFloats = 262144;  // 1 MiB
+constexpr int64_t kNoAllocScratchFloats = 262144;  // 1 MiB of partials
 
-static __device__ __align__(256) float g_noalloc_scratch[kNoAllocScratchFloats];
+static __device__ __align__(256) float g_noalloc_scratch[kHeaderFloats + kNoAllocScratchFloats];
 
 // Device address of the scratch array on the current device.  In host code
 // the array's name is only a host-side stand-in, so the address is looked up
@@ -605,9 +886,10 @@ extern "C" frt_status frt_quantize_e4m3_noalloc(const void* x, frt_dtype x_dtype
   if (!aligned(x, esize) || (scale && !aligned(scale, 4)) ||
       (static_scale && !aligned(static_scale, 4)))
     return FRT_ERR_MISALIGNED;
-  // the scratch holds at most kNoAllocScratchFloats partial maxima
+  // the scratch holds the header and at most kNoAllocScratchFloats partial maxima
   if (!static_scale && frt_quantize_workspace_bytes(rows, cols, mode) >
-                           static_cast<size_t>(kNoAllocScratchFloats) * sizeof(float))
+                           static_cast<size_t>(kHeaderFloats + kNoAllocScratchFloats) *
+                               sizeof(float))
     return FRT_ERR_UNSUPPORTED_SHAPE;
   frt_status st = FRT_OK;
   float* ws = noalloc_scratch(&st);

@@ -510,5 +510,16 @@ __device__ __forceinline__ bool wait_counter(const unsigned* ctr, unsigned targe
   }
 }
 
+// Waits until *ctr differs from `seen` (acquire), about one second at most.
+__device__ __forceinline__ bool wait_counter_change(const unsigned* ctr, unsigned seen) {
+  if (ld_acquire_gpu(ctr) != seen) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    __nanosleep(32);
+    if (ld_acquire_gpu(ctr) != seen) return true;
+    if ((it & 15u) == 0u && globaltimer_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
 }  // namespace dev
 }  // namespace frt

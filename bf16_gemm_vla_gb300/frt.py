@@ -69,7 +69,7 @@ def frt_quantize_e4m3(x, mode=PER_TENSOR, out_fmt=OCP, static_scale=None, q=None
         scale = torch.empty((cols if mode == PER_COL else 1,), dtype=torch.float32, device=x.device)
     if static_scale is None and workspace is None:
         nb = L.frt_quantize_workspace_bytes(rows, cols, _MODE[mode])
-        workspace = torch.empty((max(nb, 4) // 4,), dtype=torch.float32, device=x.device)
+        workspace = torch.zeros((max(nb, 4) // 4,), dtype=torch.float32, device=x.device)
     wsb = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check("frt_quantize_e4m3",
            L.frt_quantize_e4m3(x.data_ptr(), _XDT[x.dtype], rows, cols, ldx, _MODE[mode],

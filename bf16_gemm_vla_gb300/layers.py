@@ -74,7 +74,7 @@ class Linear:
             self.q = torch.empty((M, weight.K), dtype=torch.uint8, device=dev)
             self.a_scale = torch.empty((1,), dtype=torch.float32, device=dev)
             nb = frt.frt_quantize_workspace_bytes(M, weight.K, frt.PER_TENSOR)
-            self.ws = torch.empty((max(nb, 4) // 4,), dtype=torch.float32, device=dev)
+            self.ws = torch.zeros((max(nb, 4) // 4,), dtype=torch.float32, device=dev)
         # the GEMM's own (zero-filled) workspace, or False if it needs none
         gws = frt.gemm_workspace(M, weight.N, weight.K, weight.kind, dev)
         self.gws = False if gws is None else gws

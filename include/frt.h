@@ -102,10 +102,22 @@ const char* frt_status_string(frt_status status);
  *           column); amax is skipped and the workspace is not used.
  * q         : [rows x cols] bytes, contiguous (row stride cols).
  * scale     : device, receives s (1 float, or `cols` floats); may be NULL.
- * workspace : device scratch of frt_quantize_workspace_bytes() bytes, 4-byte
- *             aligned; its contents need no initialisation and are
- *             overwritten.  Calls that share a workspace must be ordered on
- *             one stream.
+ * workspace : device memory of frt_quantize_workspace_bytes() bytes, 4-byte
+ *             aligned (16-byte aligned to allow the one-grid path below).
+ *             Its first 256 bytes are a header that must be zero-filled
+ *             before the workspace's first use and is not written by the
+ *             caller after that: every call leaves it ready for the next.
+ *             The rest is scratch (amax partials).  Calls that share a
+ *             workspace must be ordered on one stream.
+ *             Per tensor, when x is dense (ldx == cols), 16-byte aligned and
+ *             small enough to sit on chip (in registers up to 32 KiB per SM,
+ *             else in shared memory up to 208 KiB per SM), one grid does
+ *             both passes: each CTA holds its part of x, the CTAs meet at a
+ *             barrier in the header (so the grid's CTAs, at most one per SM,
+ *             must all be resident at once), and x is read once.  A CTA that
+ *             waits there for over a second gives up: the call's scale
+ *             becomes NaN and header word 3 (bytes 12-15) nonzero; the
+ *             caller then zero-fills the header again.
  * Requires rows, cols >= 0, ldx >= cols; x, q, scale 4-byte aligned.
  * Vector paths are taken when x/q are 16-byte aligned and cols, ldx are
  * multiples of 8; other shapes take a scalar path with the same results.
@@ -125,20 +137,26 @@ frt_status frt_quantize_e4m3(const void* x, frt_dtype x_dtype, int64_t rows, int
  * plugin that only receives raw device pointers from its host application,
  * or code recording a CUDA graph in a mode where allocating would break the
  * capture.  It computes exactly what frt_quantize_e4m3 computes, with the
- * same arguments minus the workspace: the amax partials live in a fixed
- * 1 MiB array inside the library (262144 floats), which every GPU that loads
- * the library keeps until the process exits.
+ * same arguments minus the workspace: the workspace header and the amax
+ * partials live in a fixed array inside the library (256 bytes + 1 MiB,
+ * 262144 partials), which every GPU that loads the library keeps until the
+ * process exits.
  *   - Nothing is allocated or freed, by this call or by any routine it calls.
  *   - Size limit (only when static_scale is NULL): the workspace that
- *     frt_quantize_workspace_bytes() reports must be at most 1 MiB -- always
+ *     frt_quantize_workspace_bytes() reports must be at most 256 bytes +
+ *     1 MiB -- always
  *     true per tensor; per column ceil(rows / 64) * cols <= 262144.  Larger
  *     shapes return FRT_ERR_UNSUPPORTED_SHAPE and enqueue nothing.
  *   - The first call on a device looks up the array's device address (with
  *     that device current) and caches it; make that first call before any
  *     stream capture.
  *   - All calls share the one array, and each call overwrites the partials
- *     it reads, so nothing needs clearing between calls; calls that overlap
- *     on the GPU (different streams, no ordering) race on it.
+ *     it reads and leaves the header ready for the next call, so nothing needs
+ *     clearing between calls; calls that overlap on the GPU (different
+ *     streams, no ordering) race on it.  After a one-grid call that gave up
+ *     (NaN scale, see frt_quantize_e4m3) the header is not restored and
+ *     later per-tensor calls on that device are invalid until the process
+ *     restarts.
  * ---------------------------------------------------------------------- */
 frt_status frt_quantize_e4m3_noalloc(const void* x, frt_dtype x_dtype, int64_t rows, int64_t cols,
                                      int64_t ldx, frt_scale_mode mode, frt_dtype out_fmt,

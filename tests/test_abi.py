@@ -50,8 +50,8 @@ def test_sizes(lib):
     assert lib.frt_packed_weight_bytes(96, 200, _lib.FRT_E4M3_OCP) == 2 * 1 * 16384
     assert lib.frt_packed_weight_bytes(80, 136, _lib.FRT_BF16) == 2 * 2 * 16384
     assert lib.frt_packed_weight_bytes(64, 64, _lib.FRT_F32) == 0
-    assert lib.frt_quantize_workspace_bytes(50, 1024, _lib.FRT_SCALE_PER_TENSOR) == 4096
-    assert lib.frt_quantize_workspace_bytes(4096, 1024, _lib.FRT_SCALE_PER_COL) == 64 * 1024 * 4
+    assert lib.frt_quantize_workspace_bytes(50, 1024, _lib.FRT_SCALE_PER_TENSOR) == 256 + 4096
+    assert lib.frt_quantize_workspace_bytes(4096, 1024, _lib.FRT_SCALE_PER_COL) == 256 + 64 * 1024 * 4
     assert lib.frt_gemm_workspace_bytes(50, 1024, 4096, _lib.FRT_E4M3_OCP) == 0
 
 

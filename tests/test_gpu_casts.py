@@ -210,3 +210,44 @@ def test_quotients_near_rounding_midpoints(fmt, ofmt):
                                      static_scale=torch.tensor([s], device="cuda"))
         qo, _ = quantize.quantize_e4m3(xc, quantize.PER_COL, ofmt, static_scale=np.float32([s]))
         np.testing.assert_array_equal(q.cpu().numpy(), qo)
+
+
+def test_quantize_workspace_reused_across_shapes():
+    # one zero-filled workspace through a sequence of per-tensor shapes whose
+    # one-grid launches have different CTA counts (and a strided view, which
+    # takes the two-kernel path): every result is the oracle's and the
+    # header (arrivals, status) is back at zero
+    nb = frt.frt_quantize_workspace_bytes(768, 16384, frt.PER_TENSOR)
+    ws = torch.zeros((nb // 4,), dtype=torch.float32, device="cuda")
+    g = np.random.default_rng(21)
+    big = g.standard_normal((64, 1032))
+    for rows, cols in [(768, 16384), (3, 16), (50, 1024), (768, 2048), (1, 8), (768, 16384),
+                       ("strided", 0), (200, 4096)]:
+        if rows == "strided":
+            xd, xh = _dev_input(big, torch.bfloat16)
+            xd, xh = xd[:, :1024], xh[:, :1024]
+        else:
+            x = g.standard_normal((rows, cols))
+            x[g.random((rows, cols)) < 0.01] *= 50.0
+            xd, xh = _dev_input(x, torch.bfloat16)
+        q, s = frt.frt_quantize_e4m3(xd, frt.PER_TENSOR, frt.OCP, workspace=ws)
+        qo, so = quantize.quantize_e4m3(xh, quantize.PER_TENSOR, e4m3.OCP)
+        assert s.cpu().numpy()[0] == so
+        np.testing.assert_array_equal(q.cpu().numpy(), qo)
+        hdr = ws[:4].view(torch.int32).cpu().numpy()
+        assert hdr[0] == 0 and hdr[3] == 0
+
+
+@pytest.mark.parametrize("extra_row", [0, 1])
+def test_quantize_one_grid_capacity_boundary(extra_row):
+    # the largest dense bf16 tensor held in the SMs' shared memory (208 KiB
+    # per SM) and one row more (two-kernel path): both bit-exact
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    cols = 8192
+    rows = sms * 212992 // (2 * cols) + extra_row
+    bits = synth.student_t_bf16(rows * cols, seed=4).reshape(rows, cols)
+    q, s = frt.frt_quantize_e4m3(bf16_dev(bits), frt.PER_TENSOR, frt.OCP)
+    xh = synth.bf16_bits_as_f32(bits)
+    qo, so = quantize.quantize_e4m3(xh, quantize.PER_TENSOR, e4m3.OCP)
+    assert s.cpu().numpy()[0] == so
+    np.testing.assert_array_equal(q.cpu().numpy(), qo)
