@@ -373,20 +373,31 @@ __global__ void __launch_bounds__(kQThreads) encode_tensor_kernel(
 // s = amax / max (1 if amax is 0); finally every CTA encodes its part from
 // chip.  x is read from memory once.
 //
-// The barrier is a sense-reversing pair of counters: each CTA reads the
-// generation (after the previous grid has completed), folds its maximum into
-// the header's amax word (an unsigned max of the non-negative fp32 bits),
-// then arrives; the last arrival reads the amax, resets it and the arrival
-// count, publishes s and advances the generation, which releases the
-// others.  Waits are bounded; a CTA that gives up records a code in the
-// header's status word and uses s = NaN, so the result is visibly invalid.
-constexpr int kResThreads = 512;
+// The barrier is sense-reversing: each CTA reads the generation (after the
+// previous grid has completed), stores its maximum among the partials and
+// arrives on the arrival count (acquire-release); the last arrival reduces
+// the partials to s, resets the count and publishes the next generation
+// together with s in one 64-bit release store, which the others poll.
+// Waits are bounded; a CTA that gives up records a code in the header's
+// status word and uses s = NaN, so the result is visibly invalid.
+constexpr int kResThreads = 1024;
 constexpr int kResChunk = 16384;    // bytes per bulk copy
 constexpr int kResMaxChunks = 13;   // at most 208 KiB of a tensor per CTA
 constexpr int kResSmem = kResChunk * kResMaxChunks;
-constexpr int kRegVecs = 4;         // register path: 16-byte vectors per thread
+constexpr int kRegVecs = 2;         // register path: 16-byte vectors per thread
 constexpr int kHeaderFloats = 64;   // workspace header: 256 bytes
-// header words: [0] arrivals, [1] generation, [2] scale bits, [3] status, [4] amax bits
+// header words: [0] arrivals, [1] status, [2] generation and [3] scale bits
+// (one 64-bit word)
+
+__device__ __forceinline__ unsigned long long ld_acquire_gpu_u64(const unsigned* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_release_gpu_u64(unsigned* p, unsigned long long v) {
+  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
 
 __device__ __forceinline__ unsigned atom_add_acq_rel_gpu(unsigned* p, unsigned v) {
   unsigned old;
@@ -450,32 +461,48 @@ __device__ __forceinline__ float max16(const uint4& w, float m) {
 }
 
 // The grid barrier above.  m: this CTA's max |x| (valid in thread 0); g0:
-// the generation read by thread 0 after the dependency wait.  Returns s (or
-// NaN if this CTA gave up) in every thread.
+// the generation read by thread 0 after the dependency wait; red: the block
+// reduction buffer.  Returns s (or NaN if this CTA gave up) in every thread.
 template <bool kFnuz>
-__device__ __forceinline__ float grid_scale(float m, unsigned g0, unsigned* hdr, bool failed) {
+__device__ __forceinline__ float grid_scale(float m, unsigned g0, unsigned* hdr,
+                                            float* __restrict__ partial, bool failed, float* red) {
   __shared__ float s_sh;
-  __shared__ int fail_sh;
+  __shared__ int last_sh, fail_sh;
   if (threadIdx.x == 0) {
     fail_sh = failed;
-    atomicMax(hdr + 4, __float_as_uint(m));
-    if (atom_add_acq_rel_gpu(hdr, 1u) == gridDim.x - 1) {
-      const float a = __uint_as_float(dev::ld_acquire_gpu(hdr + 4));
+    partial[blockIdx.x] = m;  // ordered before the arrival by its release
+    last_sh = atom_add_acq_rel_gpu(hdr, 1u) == gridDim.x - 1;
+  }
+  __syncthreads();
+  if (last_sh) {
+    float a = 0.0f;
+    for (int i = threadIdx.x; i < static_cast<int>(gridDim.x); i += blockDim.x)
+      a = fmaxf(a, __ldcg(partial + i));
+    a = block_max(a, red);
+    if (threadIdx.x == 0) {
       const float sc = a == 0.0f ? 1.0f : __fdiv_rn(a, kFnuz ? 240.0f : 448.0f);
-      hdr[2] = __float_as_uint(sc);
-      hdr[4] = 0u;
       hdr[0] = 0u;
-      dev::counter_add_release(hdr + 1);
+      st_release_gpu_u64(hdr + 2, static_cast<unsigned long long>(g0 + 1u) |
+                                      (static_cast<unsigned long long>(__float_as_uint(sc)) << 32));
       s_sh = sc;
-    } else if (dev::wait_counter_change(hdr + 1, g0)) {
-      s_sh = __uint_as_float(__ldcg(hdr + 2));
-    } else {
-      fail_sh = 1;
     }
-    if (fail_sh) {
-      s_sh = __uint_as_float(0x7FC00000u);
-      atomicCAS(hdr + 3, 0u, 0x201u);
+  } else if (threadIdx.x == 0) {
+    const uint64_t t0 = dev::globaltimer_ns();
+    for (uint32_t it = 0;; ++it) {
+      const unsigned long long w = ld_acquire_gpu_u64(hdr + 2);
+      if (static_cast<unsigned>(w) != g0) {
+        s_sh = __uint_as_float(static_cast<unsigned>(w >> 32));
+        break;
+      }
+      if ((it & 15u) == 15u && dev::globaltimer_ns() - t0 > dev::kWaitLimitNs) {
+        fail_sh = 1;
+        break;
+      }
     }
+  }
+  if (threadIdx.x == 0 && fail_sh) {
+    s_sh = __uint_as_float(0x7FC00000u);
+    atomicCAS(hdr + 1, 0u, 0x201u);
   }
   __syncthreads();
   return s_sh;
@@ -485,11 +512,11 @@ __device__ __forceinline__ float grid_scale(float m, unsigned g0, unsigned* hdr,
 template <typename T, bool kFnuz>
 __global__ void __launch_bounds__(kResThreads) quantize_regs_kernel(
     const T* __restrict__ x, int64_t n_vec, uint8_t* __restrict__ q, float* __restrict__ scale_out,
-    unsigned* __restrict__ hdr) {
+    unsigned* __restrict__ hdr, float* __restrict__ partial) {
   constexpr int VEC = 16 / sizeof(T);
   __shared__ float red[32];
   dev::grid_dependency_wait();  // x may come from the previous grid
-  const unsigned g0 = threadIdx.x == 0 ? dev::ld_acquire_gpu(hdr + 1) : 0u;
+  const unsigned g0 = threadIdx.x == 0 ? dev::ld_acquire_gpu(hdr + 2) : 0u;
   const uint4* xv = reinterpret_cast<const uint4*>(x);
   const int64_t stride = static_cast<int64_t>(gridDim.x) * kResThreads;
   const int64_t v0 = static_cast<int64_t>(blockIdx.x) * kResThreads + threadIdx.x;
@@ -501,7 +528,8 @@ __global__ void __launch_bounds__(kResThreads) quantize_regs_kernel(
 #pragma unroll
   for (int j = 0; j < kRegVecs; ++j) m = max16<T>(w[j], m);
   m = block_max(m, red);
-  const float sc = grid_scale<kFnuz>(m, g0, hdr, false);
+  __syncthreads();  // red is reused by the barrier
+  const float sc = grid_scale<kFnuz>(m, g0, hdr, partial, false, red);
   dev::grid_launch_dependents();  // every CTA is past the barrier
   if (blockIdx.x == 0 && threadIdx.x == 0 && scale_out) *scale_out = sc;
   const float r = __frcp_rn(sc);
@@ -515,7 +543,7 @@ __global__ void __launch_bounds__(kResThreads) quantize_regs_kernel(
 template <typename T, bool kFnuz>
 __global__ void __launch_bounds__(kResThreads, 1) quantize_resident_kernel(
     const T* __restrict__ x, int64_t n, int64_t per_cta, uint8_t* __restrict__ q,
-    float* __restrict__ scale_out, unsigned* __restrict__ hdr) {
+    float* __restrict__ scale_out, unsigned* __restrict__ hdr, float* __restrict__ partial) {
   constexpr int VEC = 16 / sizeof(T);
   extern __shared__ __align__(128) uint8_t res[];
   __shared__ uint64_t bars[kResMaxChunks];
@@ -534,7 +562,7 @@ __global__ void __launch_bounds__(kResThreads, 1) quantize_resident_kernel(
   dev::grid_dependency_wait();  // x may come from the previous grid
   unsigned g0 = 0;
   if (tid == 0) {
-    g0 = dev::ld_acquire_gpu(hdr + 1);
+    g0 = dev::ld_acquire_gpu(hdr + 2);
     const uint64_t pol = dev::policy_evict_first();
     const uint8_t* src = reinterpret_cast<const uint8_t*>(x + e0);
     for (int i = 0; i < nchunks; ++i) {
@@ -555,8 +583,8 @@ __global__ void __launch_bounds__(kResThreads, 1) quantize_resident_kernel(
       m = max16<T>(*reinterpret_cast<const uint4*>(res + i * kResChunk + v * 16), m);
   }
   m = block_max(m, red);
-  const bool failed = __syncthreads_or(!ok);
-  const float sc = grid_scale<kFnuz>(m, g0, hdr, failed);
+  const bool failed = __syncthreads_or(!ok);  // also: red is reused by the barrier
+  const float sc = grid_scale<kFnuz>(m, g0, hdr, partial, failed, red);
   dev::grid_launch_dependents();  // every CTA is past the barrier
   if (blockIdx.x == 0 && tid == 0 && scale_out) *scale_out = sc;
   const float r = __frcp_rn(sc);
@@ -667,8 +695,8 @@ frt_status quantize_typed(const T* x, int64_t rows, int64_t cols, int64_t ldx, f
       attr[0].val.programmaticStreamSerializationAllowed = 1;
       cfg.attrs = attr;
       cfg.numAttrs = 1;
-      if (cudaLaunchKernelEx(&cfg, quantize_regs_kernel<T, kFnuz>, x, n_vec16, q, scale, hdr) !=
-          cudaSuccess) {
+      if (cudaLaunchKernelEx(&cfg, quantize_regs_kernel<T, kFnuz>, x, n_vec16, q, scale, hdr,
+                             ws) != cudaSuccess) {
         cudaGetLastError();
         return FRT_ERR_CUDA;
       }
@@ -695,8 +723,8 @@ frt_status quantize_typed(const T* x, int64_t rows, int64_t cols, int64_t ldx, f
       attr[0].val.programmaticStreamSerializationAllowed = 1;
       cfg.attrs = attr;
       cfg.numAttrs = 1;
-      if (cudaLaunchKernelEx(&cfg, quantize_resident_kernel<T, kFnuz>, x, n, per, q, scale,
-                             hdr) != cudaSuccess) {
+      if (cudaLaunchKernelEx(&cfg, quantize_resident_kernel<T, kFnuz>, x, n, per, q, scale, hdr,
+                             ws) != cudaSuccess) {
         cudaGetLastError();
         return FRT_ERR_CUDA;
       }

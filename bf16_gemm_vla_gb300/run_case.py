@@ -73,7 +73,7 @@ def quantize_case(a, dev):
     x = torch.randn((a.M, a.K), generator=g, device=dev).to(torch.bfloat16)
     q = torch.empty((a.M, a.K), dtype=torch.uint8, device=dev)
     s = torch.empty((1,), dtype=torch.float32, device=dev)
-    ws = torch.empty((4096,), dtype=torch.float32, device=dev)
+    ws = torch.zeros((4096,), dtype=torch.float32, device=dev)  # header zero-filled once
     one = torch.ones((1,), dtype=torch.float32, device=dev)
 
     def once():

@@ -116,7 +116,7 @@ const char* frt_status_string(frt_status status);
  *             barrier in the header (so the grid's CTAs, at most one per SM,
  *             must all be resident at once), and x is read once.  A CTA that
  *             waits there for over a second gives up: the call's scale
- *             becomes NaN and header word 3 (bytes 12-15) nonzero; the
+ *             becomes NaN and header word 1 (bytes 4-7) nonzero; the
  *             caller then zero-fills the header again.
  * Requires rows, cols >= 0, ldx >= cols; x, q, scale 4-byte aligned.
  * Vector paths are taken when x/q are 16-byte aligned and cols, ldx are
