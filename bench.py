@@ -239,6 +239,17 @@ def capture(fn):
     return g
 
 
+def launches_of(fn):
+    """Kernels of this library that one call of fn() launches (its launch
+    counter around the call)."""
+    from bf16_gemm_vla_gb300 import frt
+
+    n0 = frt.frt_launch_count()
+    fn()
+    torch.cuda.synchronize()
+    return frt.frt_launch_count() - n0
+
+
 def l2_bytes():
     return int(getattr(torch.cuda.get_device_properties(torch.cuda.current_device()),
                        "L2_cache_size", 128 << 20))
@@ -356,6 +367,7 @@ def run_headline(args, device, world, sampler, peaks, peak_kind):
     sets = [set0] + [EncoderFP8Set(list(zip(set0.layers, set0.inputs)), device)
                      for _ in range(R - 1)]
     torch.cuda.synchronize()  # weight copies complete before the GEMMs read them
+    launches_per_step = launches_of(set0.forward)  # what one replay of a step graph runs
     graphs = [capture(s.forward) for s in sets]
     flops = set0.flops()
     for i in range(args.warmup):
@@ -440,7 +452,7 @@ def run_headline(args, device, world, sampler, peaks, peak_kind):
         "roofline": roofline, "layers": layers_out,
         "e2e": {"value": e2e_value / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps},
-        "launches_per_step": 3 * len(set0.layers),
+        "launches_per_step": launches_per_step,
     }
 
 
@@ -513,7 +525,7 @@ def run_components(args, device, sampler, peaks):
     x = bf16_to_dev(synth.student_t_bf16(n, seed=3).reshape(-1, 4096), device)
     q = torch.empty(x.shape, dtype=torch.uint8, device=device)
     s = torch.empty(1, dtype=torch.float32, device=device)
-    ws = torch.empty(frt.frt_quantize_workspace_bytes(x.shape[0], x.shape[1]) // 4,
+    ws = torch.zeros(frt.frt_quantize_workspace_bytes(x.shape[0], x.shape[1]) // 4,
                      dtype=torch.float32, device=device)
 
     def quant(i):
@@ -551,7 +563,7 @@ def run_components(args, device, sampler, peaks):
     sampler.window(t0, time.time())
     frt.check_device_status()
     out["stack_18enc_fp8_18dec_bf16"] = {"ms_per_replay": secs * 1e3,
-                                         "launches_per_replay": st.launches_per_forward(),
+                                         "launches_per_replay": launches_of(st.forward),
                                          "weight_bytes": st.weight_bytes()}
     del st
     torch.cuda.empty_cache()
@@ -690,7 +702,8 @@ def main(argv=None):
             "ms_per_step": head["secs"] / args.steps * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "e4m3", "data": "synthetic",
             "config": head["config"], "roofline": head["roofline"], "cpu_baseline": cpu,
-            "e2e": head["e2e"], "gpu_launches": head["launches_per_step"] * args.steps,
+            "e2e": head["e2e"],
+            "gpu_launches": head["launches_per_step"] * args.steps,
             "clocks": clocks, "layers": head["layers"], "components": comps,
             "peaks": {"source": peak_kind, "hbm_gbs": peaks["hbm_gbs"],
                       "bf16_tflops": peaks["bf16_tflops"],

@@ -33,6 +33,7 @@ _c_int = ctypes.c_int
 # name -> (restype, argtypes), in the order of include/frt.h
 SIGNATURES = {
     "frt_abi_version": (_c_int, []),
+    "frt_launch_count": (ctypes.c_ulonglong, []),
     "frt_status_string": (ctypes.c_char_p, [_c_int]),
     "frt_quantize_workspace_bytes": (_c_sz, [_c_i64, _c_i64, _c_int]),
     "frt_quantize_e4m3": (_c_int, [_c_p, _c_int, _c_i64, _c_i64, _c_i64, _c_int, _c_int, _c_p,

@@ -700,6 +700,7 @@ frt_status quantize_typed(const T* x, int64_t rows, int64_t cols, int64_t ldx, f
         cudaGetLastError();
         return FRT_ERR_CUDA;
       }
+      note_launches(1);
       return launch_status();
     }
     if (!static_scale && vec && ldx == cols && aligned(ws_all, 16) &&
@@ -728,6 +729,7 @@ frt_status quantize_typed(const T* x, int64_t rows, int64_t cols, int64_t ldx, f
         cudaGetLastError();
         return FRT_ERR_CUDA;
       }
+      note_launches(1);
       return launch_status();
     }
     const int64_t total = rows * (vec ? cols / 8 : cols);
@@ -765,6 +767,7 @@ frt_status quantize_typed(const T* x, int64_t rows, int64_t cols, int64_t ldx, f
       cudaGetLastError();
       return FRT_ERR_CUDA;
     }
+    note_launches(static_scale ? 1 : 2);
   } else {
     const dim3 grid(static_cast<unsigned>(ceil_div(cols, kQThreads)),
                     static_cast<unsigned>(ceil_div(rows, kColRowsPerBlock)));
@@ -772,6 +775,7 @@ frt_status quantize_typed(const T* x, int64_t rows, int64_t cols, int64_t ldx, f
     encode_col_kernel<T, kFnuz><<<grid, kQThreads, 0, st>>>(x, rows, cols, ldx, ws,
                                                              static_cast<int>(grid.y),
                                                              static_scale, q, scale);
+    note_launches(static_scale ? 1 : 2);
   }
   return launch_status();
 }
@@ -841,13 +845,18 @@ extern "C" frt_status frt_fnuz_to_ocp(const uint8_t* in, uint8_t* out, size_t n,
       const int grid = static_cast<int>(want < cap ? want : cap);
       fnuz_to_ocp_vec_kernel<<<grid, 256, 0, st>>>(reinterpret_cast<const uint4*>(in),
                                                    reinterpret_cast<uint4*>(out), n16);
+      note_launches(1);
     }
     const size_t tail = n - n16 * 16;
-    if (tail) fnuz_to_ocp_byte_kernel<<<1, 32, 0, st>>>(in + n16 * 16, out + n16 * 16, tail);
+    if (tail) {
+      fnuz_to_ocp_byte_kernel<<<1, 32, 0, st>>>(in + n16 * 16, out + n16 * 16, tail);
+      note_launches(1);
+    }
   } else {
     const int64_t want = ceil_div(static_cast<int64_t>(n), 256);
     const int grid = static_cast<int>(want < cap ? want : cap);
     fnuz_to_ocp_byte_kernel<<<grid, 256, 0, st>>>(in, out, n);
+    note_launches(1);
   }
   return launch_status();
 }

@@ -1,4 +1,5 @@
-// Status strings, ABI version and device queries.
+// Status strings, ABI version, device queries and the launch counter.
+#include <atomic>
 #include <mutex>
 
 #include "frt_host.h"
@@ -19,9 +20,17 @@ int sm_count() {
   return counts[dev];
 }
 
+namespace {
+std::atomic<unsigned long long> g_launches{0};
+}  // namespace
+
+void note_launches(int n) { g_launches.fetch_add(static_cast<unsigned long long>(n)); }
+
 }  // namespace frt
 
 extern "C" int frt_abi_version(void) { return 1; }
+
+extern "C" unsigned long long frt_launch_count(void) { return frt::g_launches.load(); }
 
 extern "C" const char* frt_status_string(frt_status s) {
   switch (s) {

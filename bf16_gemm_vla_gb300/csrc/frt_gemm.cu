@@ -1132,7 +1132,9 @@ cudaError_t launch_one(const CUtensorMap& ta, const CUtensorMap& tw, const CUten
   attr[1].val.clusterDim.z = pl.split_global ? 1 : pl.splits;
   cfg.attrs = attr;
   cfg.numAttrs = (kPair || pl.splits > 1) ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, kern, ta, tw, to, a);
+  e = cudaLaunchKernelEx(&cfg, kern, ta, tw, to, a);
+  if (e == cudaSuccess) note_launches(1);
+  return e;
 }
 
 template <bool kFp8>

@@ -24,4 +24,8 @@ inline frt_status launch_status() {
 // Number of SMs of the current device (cached per device ordinal).
 int sm_count();
 
+// Adds n to the count of kernels this library has launched (or recorded
+// into a stream capture); see frt_launch_count.
+void note_launches(int n);
+
 }  // namespace frt

@@ -117,5 +117,6 @@ extern "C" frt_status frt_pack_weights(const void* w, frt_dtype w_dtype, int64_t
   else
     pack_kernel<__nv_bfloat16, 2><<<grid, kPackThreads, 0, st>>>(
         static_cast<const __nv_bfloat16*>(w), K, N, ldw, kb_total, out);
+  note_launches(1);
   return launch_status();
 }

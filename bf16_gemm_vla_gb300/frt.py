@@ -53,6 +53,11 @@ def _rows_view(x, name):
 
 # ---------------------------------------------------------------- quantize
 
+def frt_launch_count():
+    """Kernels this library has launched (or recorded into a capture) so far."""
+    return lib().frt_launch_count()
+
+
 def frt_quantize_workspace_bytes(rows, cols, mode=PER_TENSOR):
     return lib().frt_quantize_workspace_bytes(rows, cols, _MODE[mode])
 

@@ -97,7 +97,7 @@ class SyntheticStack:
         for chain in (self.enc, self.dec):
             for lay in chain:
                 for lin in lay.values():
-                    n += 3 if lin.w.kind == "e4m3" else 1  # amax + encode + GEMM
+                    n += 2 if lin.w.kind == "e4m3" else 1  # quantize (one grid) + GEMM
         return n
 
     def capture(self):

@@ -78,6 +78,11 @@ typedef enum {
 /* Version of this ABI (incremented on any signature change). */
 int frt_abi_version(void);
 
+/* Number of kernels this library has launched in this process (or recorded
+ * into a stream capture: a captured call counts once, its graph's replays do
+ * not), over all devices and threads.  For accounting only. */
+unsigned long long frt_launch_count(void);
+
 /* Human-readable name of a status code (static string, never NULL). */
 const char* frt_status_string(frt_status status);
 
