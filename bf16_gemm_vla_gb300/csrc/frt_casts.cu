@@ -380,11 +380,12 @@ __global__ void __launch_bounds__(kQThreads) encode_tensor_kernel(
 // together with s in one 64-bit release store, which the others poll.
 // Waits are bounded; a CTA that gives up records a code in the header's
 // status word and uses s = NaN, so the result is visibly invalid.
-constexpr int kResThreads = 1024;
+constexpr int kResThreads = 1024;   // shared-memory path
+constexpr int kRegThreads = 512;    // register path
 constexpr int kResChunk = 16384;    // bytes per bulk copy
 constexpr int kResMaxChunks = 13;   // at most 208 KiB of a tensor per CTA
 constexpr int kResSmem = kResChunk * kResMaxChunks;
-constexpr int kRegVecs = 2;         // register path: 16-byte vectors per thread
+constexpr int kRegVecs = 3;         // register path: 16-byte vectors per thread
 constexpr int kHeaderFloats = 64;   // workspace header: 256 bytes
 // header words: [0] arrivals, [1] status, [2] generation and [3] scale bits
 // (one 64-bit word)
@@ -509,17 +510,21 @@ __device__ __forceinline__ float grid_scale(float m, unsigned g0, unsigned* hdr,
 }
 
 // Register path: thread t of CTA b holds vectors t + 512 (b + G j), j < kRegVecs.
+// A CTA takes at most 512 x 48 registers and no shared memory, so a GEMM CTA
+// (the usual next grid) fits beside it: the next grid is let go at once,
+// and its prologue and weight prefetch overlap this grid.
 template <typename T, bool kFnuz>
-__global__ void __launch_bounds__(kResThreads) quantize_regs_kernel(
+__global__ void __maxnreg__(48) quantize_regs_kernel(
     const T* __restrict__ x, int64_t n_vec, uint8_t* __restrict__ q, float* __restrict__ scale_out,
     unsigned* __restrict__ hdr, float* __restrict__ partial) {
   constexpr int VEC = 16 / sizeof(T);
   __shared__ float red[32];
+  dev::grid_launch_dependents();
   dev::grid_dependency_wait();  // x may come from the previous grid
   const unsigned g0 = threadIdx.x == 0 ? dev::ld_acquire_gpu(hdr + 2) : 0u;
   const uint4* xv = reinterpret_cast<const uint4*>(x);
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * kResThreads;
-  const int64_t v0 = static_cast<int64_t>(blockIdx.x) * kResThreads + threadIdx.x;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * kRegThreads;
+  const int64_t v0 = static_cast<int64_t>(blockIdx.x) * kRegThreads + threadIdx.x;
   uint4 w[kRegVecs];
 #pragma unroll
   for (int j = 0; j < kRegVecs; ++j)
@@ -530,7 +535,6 @@ __global__ void __launch_bounds__(kResThreads) quantize_regs_kernel(
   m = block_max(m, red);
   __syncthreads();  // red is reused by the barrier
   const float sc = grid_scale<kFnuz>(m, g0, hdr, partial, false, red);
-  dev::grid_launch_dependents();  // every CTA is past the barrier
   if (blockIdx.x == 0 && threadIdx.x == 0 && scale_out) *scale_out = sc;
   const float r = __frcp_rn(sc);
   const bool fast_ok = recip_is_normal(sc, r);
@@ -682,13 +686,13 @@ frt_status quantize_typed(const T* x, int64_t rows, int64_t cols, int64_t ldx, f
     const int sms = sm_count() > 0 ? sm_count() : 148;
     const int64_t n_vec16 = n * static_cast<int64_t>(sizeof(T)) / 16;
     if (!static_scale && vec && ldx == cols && aligned(ws_all, 16) &&
-        n_vec16 <= static_cast<int64_t>(sms) * kResThreads * kRegVecs) {
+        n_vec16 <= static_cast<int64_t>(sms) * kRegThreads * kRegVecs) {
       // one grid, the tensor in registers: at most one CTA per SM
       const int grid = static_cast<int>(
-          std::min<int64_t>(sms, ceil_div(n_vec16, static_cast<int64_t>(kResThreads))));
+          std::min<int64_t>(sms, ceil_div(n_vec16, static_cast<int64_t>(kRegThreads))));
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(grid);
-      cfg.blockDim = dim3(kResThreads);
+      cfg.blockDim = dim3(kRegThreads);
       cfg.stream = st;
       cudaLaunchAttribute attr[1];
       attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

@@ -439,10 +439,11 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const void* tmap,
 }
 
 // Arrival on an mbarrier of another CTA of the cluster (address from
-// map_to_rank), ordered after this thread's earlier memory operations.
+// map_to_rank), with the default (CTA-scope release) semantics.  Used to
+// hand a drained TMEM accumulator back: the TMEM reads it follows have
+// completed (tcgen05.wait::ld) and are ordered by tcgen05.fence.
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster)
-               : "memory");
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
 }
 
 // mbar_wait for phases completed by arrivals from other CTAs of the cluster

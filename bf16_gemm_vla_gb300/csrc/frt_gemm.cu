@@ -82,6 +82,8 @@ struct GemmArgs {
   int recv_off;
   int tail_off;        // per-channel scale/bias, then mbarriers
   int split_global;    // split-K partials exchanged through the workspace (pairs)
+  __nv_bfloat16* out;  // small M: output rows stored straight from registers
+  int ldo;
   float* ws_part;      // split_global: partial chunks, one slot per (tile, CTA, chunk, split)
   unsigned* ws_flag;   // split_global: per (tile, CTA, owner split) arrival counters
   int* dev_status;
@@ -165,6 +167,19 @@ __device__ __forceinline__ void warp_store(const float* v, uint8_t* buf, uint32_
   }
 }
 
+// Small M: stores kRows output rows of one channel straight from registers
+// (v[j] = row y0 + j; the lanes of a warp hold consecutive channels, so each
+// row's store instruction covers 64 contiguous bytes).  Rows >= M and
+// channels >= N are not written.
+template <int kRows>
+__device__ __forceinline__ void store_rows(const float* v, const GemmArgs& p, int y0, int n) {
+  if (n >= p.N) return;
+  __nv_bfloat16* dst = p.out + static_cast<size_t>(y0) * p.ldo + n;
+#pragma unroll
+  for (int j = 0; j < kRows; ++j)
+    if (y0 + j < p.M) dst[static_cast<size_t>(j) * p.ldo] = __float2bfloat16_rn(v[j]);
+}
+
 // Byte offset of float4 granule q of row r in a split-K partial chunk of
 // 128 rows x cw floats (cw = 32 or 8); granules are XOR-swizzled by row so
 // that row-per-thread reads and writes are free of bank conflicts.
@@ -182,8 +197,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int kEsize = kFp8 ? 1 : 2;
   const int stages = p.stages;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* base = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  // 1024-byte aligned base, by pointer arithmetic on the shared array so
+  // that accesses through it stay shared-memory loads and stores
+  uint8_t* base = smem_raw + ((1024u - (dev::smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sbase = dev::smem_u32(base);
   float* col_sb = reinterpret_cast<float*>(base + p.tail_off);  // [2 bufs][scale, bias][kBN]
   uint64_t* bars = reinterpret_cast<uint64_t*>(col_sb + 4 * kBN);
@@ -210,6 +226,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                           : (kPair ? static_cast<int>(crank >> 1) : static_cast<int>(crank));
   const bool leader = px == 0;  // issues the pair's MMAs
   const uint32_t lead_rank = crank & ~1u;
+  // A pair without a cluster split meets once more before it frees TMEM.
+  // Each warp arrives on that barrier as soon as it is done with everything
+  // that crosses to the other CTA (the copy warp after its drain, the MMA
+  // warp after its last commit, the epilogue after the last accumulator is
+  // ready), all lanes together, and waits at the very end.  The arrivals
+  // carry no memory ordering: the data that crosses was already ordered by
+  // the mbarriers; this barrier only keeps either CTA from leaving early.
+  const bool early_bye = kPair && !csplit;
   // cluster rank of the CTA that holds K split j of this CTA's rows
   auto split_cta = [&](int j) -> uint32_t {
     return kPair ? static_cast<uint32_t>(2 * j + px) : static_cast<uint32_t>(j);
@@ -393,6 +417,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     __syncwarp();
+    if (early_bye) dev::cluster_arrive_relaxed();
   } else if (warp == 1) {
     if (lane == 0 && leader) {
       // ------------------------------------------------------------ MMA
@@ -448,6 +473,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     __syncwarp();
+    if (early_bye) dev::cluster_arrive_relaxed();
   } else {
     // -------------------------------------------------------------- epilogue
     const int et = threadIdx.x - 64;  // 0..127
@@ -458,6 +484,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t wbuf_s = sbase + p.outbuf_off + (warp - 2) * 2 * kWarpOutBytes;
     int wb = 0;
     bool ok = true;
+    bool bye = false;  // arrived on the pair's final cluster barrier
     // a drained accumulator buffer goes back to the MMA issuer (the leader
     // of a pair, whose MMAs write both CTAs' TMEM)
     auto release_acc = [&](int b) {
@@ -488,6 +515,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = dev::mbar_wait(tfull0 + 8 * b, u & 1, abort_flag, p.dev_status,
                           dev::kTimeoutEpilogue);
       ok = __all_sync(0xffffffffu, ok);
+      if (early_bye && it + 1 == my_tiles) {
+        dev::cluster_arrive_relaxed();
+        bye = true;
+      }
       dev::tc_fence_after();
       const uint32_t tacc = tmem + lane_off + static_cast<uint32_t>(b * kBN);
       // the activation scale comes from the previous grid: read it only now
@@ -544,8 +575,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int j = 0; j < 32; ++j) v[j] = gelu_tanh(v[j]);
           }
-          warp_store<true, 32>(v, wbuf + wb * kWarpOutBytes, wbuf_s + wb * kWarpOutBytes,
-                               &tmap_out, tn * kTile + ew * 32, rows_of_tile_m0 + c32, lane);
+          store_rows<32>(v, p, rows_of_tile_m0 + c32, tn * kTile + row);
         }
         wb ^= 1;
       };
@@ -556,14 +586,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int c = 0; c < kBN; c += 64) {
             float v[64];
             dev::tmem_ld64(tacc + c, v);
-            if (c + 64 == kBN) release_acc(b);  // accumulator read out
+            // accumulator read out: back to the MMA unless this was the last tile
+            if (c + 64 == kBN && it + 1 < my_tiles) release_acc(b);
             finish32(v, c, tm * kBN);
             finish32(v + 32, c + 32, tm * kBN);
           }
         } else {
           float v[32];
           dev::tmem_ld32(tacc, v);
-          release_acc(b);
+          if (it + 1 < my_tiles) release_acc(b);
           finish32(v, 0, tm * kBN);
         }
       } else if (gsplit) {
@@ -719,8 +750,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         dev::cluster_arrive_relaxed();  // phase 2: every copy into this CTA has landed
         const uint8_t* recv = base + p.recv_off;
         if constexpr (kSwap) {
-          // all owned rows of this warp are staged first (rows lc*8.. of the
-          // warp's two 32-row buffers), then one fence and one store per chunk
 #pragma unroll 1
           for (int lc = 0; lc < owned; ++lc) {
             float own[8];
@@ -751,24 +780,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
               for (int j = 0; j < 8; ++j) sum[j] = gelu_tanh(sum[j]);
             }
-            uint8_t* buf = wbuf + ((lc * 8) >> 5) * kWarpOutBytes;
-            const int r0 = (lc * 8) & 31;
-            const int cb = lane * 2;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const int rr = r0 + j;
-              *reinterpret_cast<__nv_bfloat16*>(buf + rr * 64 + (((cb >> 4) ^ ((rr >> 1) & 3)) << 4) +
-                                                (cb & 15)) = __float2bfloat16_rn(sum[j]);
-            }
-          }
-          dev::fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            for (int lc = 0; lc < owned; ++lc)
-              dev::tma_store_2d(&tmap_out,
-                                wbuf_s + ((lc * 8) >> 5) * kWarpOutBytes + ((lc * 8) & 31) * 64,
-                                tn * kTile + ew * 32, tm * kBN + (own_c0 + lc) * 8);
-            dev::bulk_commit();
+            store_rows<8>(sum, p, tm * kBN + (own_c0 + lc) * 8, tn * kTile + row);
           }
         } else {
           for (int c = own_c0; c < own_c1; ++c) {
@@ -802,6 +814,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) break;
     }
+    if (early_bye && !bye) dev::cluster_arrive_relaxed();
     if (lane == 0) dev::bulk_wait_all();  // stores complete before the grid ends
   }
 
@@ -816,8 +829,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     dev::cluster_wait();
   } else if constexpr (kPair) {
     // neither CTA of a pair leaves (or frees TMEM) while the other may still
-    // take part in its MMAs or signal its barriers
-    dev::cluster_arrive();
+    // take part in its MMAs or signal its barriers (every warp arrived above)
     dev::cluster_wait();
   }
   dev::tc_fence_before();
@@ -867,12 +879,12 @@ struct Plan {
   dim3 grid;
 };
 
-// Shared-memory layout for a given depth; false if it does not fit.
-bool layout(Plan& pl, int stage_bytes) {
+// Shared-memory layout for a given depth; false if it needs more than `cap`.
+bool layout(Plan& pl, int stage_bytes, int cap = kSmemMax) {
   const int pipe = pl.stages * stage_bytes;
   pl.outbuf_off = pipe;
   pl.recv_off = 0;
-  int tail = pipe + kOutBytes;
+  int tail = pipe + (pl.swap ? 0 : kOutBytes);  // small M stores from registers
   if (pl.splits > 1 && !pl.split_global) {
     const int nchunks = pl.bn / pl.chunk_cols;
     const int chunk = kTile * pl.chunk_cols * 4;
@@ -891,7 +903,7 @@ bool layout(Plan& pl, int stage_bytes) {
   }
   pl.tail_off = static_cast<int>(ceil_div(tail, 128) * 128);
   pl.smem = 1024 + pl.tail_off + 16 * pl.bn + kBarRegion;
-  return pl.smem <= kSmemMax;
+  return pl.smem <= cap;
 }
 
 // Sets the kernel's dynamic shared memory limit once per device.
@@ -973,7 +985,7 @@ int cluster_capacity_for(const Plan& pl, int s, int smem) {
 // Places the pipeline and the split-K receive buffers: the deepest pipeline
 // (up to `want` stages) with a dedicated receive region, or with the
 // receive buffers inside the stage buffers if that allows a deeper one.
-bool place_buffers(Plan& pl, int stage_bytes, int want) {
+bool place_buffers(Plan& pl, int stage_bytes, int want, int cap = kSmemMax) {
   int best = 0;
   bool best_in_stages = false;
   for (int mode = 0; mode < (pl.splits > 1 && !pl.split_global ? 2 : 1); ++mode) {
@@ -981,7 +993,7 @@ bool place_buffers(Plan& pl, int stage_bytes, int want) {
     for (int st = kMaxStages; st >= 2; --st) {
       if (!pl.recv_in_stages && st > want) continue;
       pl.stages = st;
-      if (!layout(pl, stage_bytes)) continue;
+      if (!layout(pl, stage_bytes, cap)) continue;
       const int eff = st < want ? st : want;
       if (eff > best) {
         best = eff;
@@ -994,7 +1006,7 @@ bool place_buffers(Plan& pl, int stage_bytes, int want) {
   pl.recv_in_stages = best_in_stages;
   for (int st = best_in_stages ? kMaxStages : want; st >= 2; --st) {
     pl.stages = st;
-    if (layout(pl, stage_bytes)) return true;
+    if (layout(pl, stage_bytes, cap)) return true;
   }
   return false;
 }
@@ -1165,6 +1177,7 @@ frt_status gemm_common(bool fp8, const void* a, int64_t lda, const float* a_scal
   if (M < 1 || N < 1 || K < 1) return FRT_ERR_INVALID_ARG;
   if (act == FRT_ACT_GELU_TANH && (act_cols < 0 || act_cols > N)) return FRT_ERR_INVALID_ARG;
   if (lda < K || ldo < N) return FRT_ERR_INVALID_ARG;
+  if (ldo > (1LL << 31) - 1) return FRT_ERR_UNSUPPORTED_SHAPE;
   if (N % 16 != 0 || K % (fp8 ? 32 : 16) != 0) return FRT_ERR_UNSUPPORTED_SHAPE;
   if (M > (1LL << 31) - 1 || N > (1LL << 31) - 1 || K > (1LL << 31) - 1)
     return FRT_ERR_UNSUPPORTED_SHAPE;
@@ -1249,6 +1262,8 @@ frt_status gemm_common(bool fp8, const void* a, int64_t lda, const float* a_scal
   ga.recv_off = pl.recv_off;
   ga.tail_off = pl.tail_off;
   ga.split_global = pl.split_global ? 1 : 0;
+  ga.out = static_cast<__nv_bfloat16*>(out);
+  ga.ldo = static_cast<int>(ldo);
   ga.ws_flag = pl.split_global ? static_cast<unsigned*>(workspace) : nullptr;
   ga.ws_part = pl.split_global
                    ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + pl.ws_flag_bytes)

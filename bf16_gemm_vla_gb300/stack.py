@@ -24,7 +24,7 @@ seeded torch generator, one layer after another in the order above.
 """
 import torch
 
-from . import layers
+from . import frt, layers
 
 ENCODER = (("qkv", 2048, 2560, 0), ("o", 2048, 2048, 0), ("gate_up", 2048, 32768, 16384),
            ("down", 16384, 2048, 0))
@@ -93,12 +93,13 @@ class SyntheticStack:
         return e, d
 
     def launches_per_forward(self):
-        n = 0
-        for chain in (self.enc, self.dec):
-            for lay in chain:
-                for lin in lay.values():
-                    n += 2 if lin.w.kind == "e4m3" else 1  # quantize (one grid) + GEMM
-        return n
+        """Kernels one forward launches, counted by the library (an FP8
+        layer's quantize takes one grid when its input is dense and fits on
+        chip, else two; every GEMM is one)."""
+        n0 = frt.frt_launch_count()
+        self.forward()
+        torch.cuda.synchronize(self.device)
+        return frt.frt_launch_count() - n0
 
     def capture(self):
         """Records one forward into a CUDA graph (after one eager warm-up that

@@ -115,7 +115,7 @@ const char* frt_status_string(frt_status status);
  *             The rest is scratch (amax partials).  Calls that share a
  *             workspace must be ordered on one stream.
  *             Per tensor, when x is dense (ldx == cols), 16-byte aligned and
- *             small enough to sit on chip (in registers up to 32 KiB per SM,
+ *             small enough to sit on chip (in registers up to 24 KiB per SM,
  *             else in shared memory up to 208 KiB per SM), one grid does
  *             both passes: each CTA holds its part of x, the CTAs meet at a
  *             barrier in the header (so the grid's CTAs, at most one per SM,
