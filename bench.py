@@ -414,31 +414,75 @@ def run_headline(args, device, world, sampler, peaks, peak_kind):
                                % (peak_kind, FP8_OVER_BF16, peak_kind),
                 "per_launch_flops": tot_flops / len(set0.layers)}
 
-    # end to end through the public API: pinned host inputs -> device, graph
-    # replay, outputs -> pinned host, every step
+    # end to end through the public API: every step copies its inputs from
+    # pinned host memory, replays its graph and reads its outputs back to
+    # pinned host memory.  Steps are pipelined over three streams (inputs
+    # up, graph, outputs down) with the R buffer sets in rotation: a set is
+    # refilled only after its previous step's graph has read it, and
+    # recomputed only after that step's outputs have been read.
     h_in = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in set0.inputs]
     for h, x in zip(h_in, set0.inputs):
         h.copy_(x)
-    h_out = [torch.empty(l.out.shape, dtype=l.out.dtype, pin_memory=True) for l in set0.layers]
+    h_out = [[torch.empty(l.out.shape, dtype=l.out.dtype, pin_memory=True) for l in st.layers]
+             for st in sets]
     h2d = sum(h.numel() * h.element_size() for h in h_in)
-    d2h = sum(h.numel() * h.element_size() for h in h_out)
+    d2h = sum(h.numel() * h.element_size() for h in h_out[0])
+    up, run, down = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    ev = lambda: torch.cuda.Event()  # noqa: E731
+    computed = [ev() for _ in range(R)]  # graph of the set's last step done
+    read_back = [ev() for _ in range(R)]  # outputs of the set's last step read
+    used = [False] * R
 
     def e2e_step(i):
-        st = sets[i % R]
-        for h, x in zip(h_in, st.inputs):
-            x.copy_(h, non_blocking=True)
-        graphs[i % R].replay()
-        for h, lin in zip(h_out, st.layers):
-            h.copy_(lin.out, non_blocking=True)
+        r = i % R
+        st = sets[r]
+        filled = ev()
+        with torch.cuda.stream(up):
+            if used[r]:
+                up.wait_event(computed[r])
+            for h, x in zip(h_in, st.inputs):
+                x.copy_(h, non_blocking=True)
+            filled.record(up)
+        with torch.cuda.stream(run):
+            run.wait_event(filled)
+            if used[r]:
+                run.wait_event(read_back[r])
+            graphs[r].replay()
+            computed[r].record(run)
+        with torch.cuda.stream(down):
+            down.wait_event(computed[r])
+            for h, lin in zip(h_out[r], st.layers):
+                h.copy_(lin.out, non_blocking=True)
+            read_back[r].record(down)
+        used[r] = True
+
+    def e2e_run(n):
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(up)
+        run.wait_event(e0)
+        down.wait_event(e0)
+        for i in range(n):
+            e2e_step(i)
+        for s_ in (up, run):
+            down.wait_stream(s_)
+        e1.record(down)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / 1e3
 
     e2e_steps = max(10, min(args.steps, 500))
-    for i in range(min(args.warmup, 5)):
-        e2e_step(i)
+    e2e_run(min(max(args.warmup, R), 2 * R))
     barrier(world)
     t0 = time.time()
-    e2e_secs = device_time(e2e_step, e2e_steps)
+    e2e_secs = e2e_run(e2e_steps)
     sampler.window(t0, time.time())
     e2e_value, _ = aggregate(flops * e2e_steps, e2e_secs, world, device)
+    # every step's outputs reached the host: the last step's equal the device's
+    r_last = (e2e_steps - 1) % R
+    for h, lin in zip(h_out[r_last], sets[r_last].layers):
+        if not torch.equal(h, lin.out.cpu()):
+            raise RuntimeError("end-to-end outputs differ from the device's")
 
     cfg = {"workload": ENC_WORKLOAD, "M": M_ENC,
            "layers": [[lin.w.K, lin.w.N] for lin in set0.layers],
@@ -451,7 +495,9 @@ def run_headline(args, device, world, sampler, peaks, peak_kind):
         "value": value / 1e12, "secs": secs_max, "flops_per_step": flops, "config": cfg,
         "roofline": roofline, "layers": layers_out,
         "e2e": {"value": e2e_value / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                "pipelining": "inputs up, graph and outputs down on three streams, %d buffer "
+                              "sets in rotation" % R},
         "launches_per_step": launches_per_step,
     }
 

@@ -288,7 +288,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   // cluster-barrier arrive and wait in this kernel is executed by all 32
   // lanes of a warp together.)
   if constexpr (kPair) {
-    dev::cluster_arrive();
+    // the initialisation is published by fence.mbarrier_init (a release);
+    // the arrival itself needs no ordering
+    dev::cluster_arrive_relaxed();
     dev::cluster_wait();
   }
   // Split-K cluster barrier, phase 1: with dedicated receive buffers every
