@@ -9,8 +9,13 @@
 // contraction, the action decoder's few dozen rows make the GEMM stream its
 // weights.  One kernel template serves both on GB300:
 //
-//   * large M ("normal" tiles): MMA M = 128 activation rows, MMA N = 256
-//     output channels;
+//   * large M: 256-row tiles on CTA pairs (cta_group::2).  The two CTAs of a
+//     cluster whose ranks differ in bit 0 each hold 128 activation rows and
+//     half of the tile's 256 (or 128) output channels per k-block; the even
+//     CTA issues one tcgen05.mma with M = 256 that reads both CTAs' shared
+//     memory and writes each CTA's 128 accumulator rows into its own TMEM.
+//     Per k-block a CTA ingests 32 KiB for 128 x 256 x 128 MACs instead of
+//     48 KiB for a single-CTA 128 x 256 tile.
 //   * small M ("swap" tiles): the product is taken transposed,
 //     out^T = W^T . A^T, so the MMA's 128 rows cover output channels and
 //     the few activation rows become the MMA N dimension (32/64/128).  The
@@ -19,22 +24,23 @@
 //
 // Both operands are K-major with the 128-byte swizzle.  Activations arrive
 // by TMA (zero fill past M and K); weights are pre-packed into the exact
-// shared-memory image (frt_pack.cu) and arrive by plain bulk copies.  Warp
-// roles: warp 0 issues the copies, one thread of warp 1 issues tcgen05.mma
-// into TMEM, warps 2-5 run the epilogue, which stages bf16 results in
-// swizzled shared memory and writes them with TMA tensor stores.
+// shared-memory image (frt_pack.cu) and arrive by bulk copies (single CTA)
+// or by TMA over the packed buffer (pairs).  Warp roles: warp 0 issues the
+// copies, one thread of warp 1 issues tcgen05.mma into TMEM, warps 2-5 run
+// the epilogue (large M: bf16 staged in swizzled shared memory and written
+// by TMA tensor stores; small M: stored straight from registers).
 //
 // Scheduling:
-//   * without split-K the grid is persistent (one CTA per SM walks a
-//     strided tile list) and the TMEM accumulator is double-buffered, so a
+//   * without split-K the grid is persistent (one CTA, or pair, per SM walks
+//     a strided tile list) and the TMEM accumulator is double-buffered, so a
 //     tile's epilogue overlaps the next tile's mainloop;
-//   * when there are fewer output tiles than SMs, K is split across the
-//     CTAs of a thread-block cluster.  The tile's columns are cut into
-//     chunks, each owned by one CTA; every CTA pushes the chunks it does not
-//     own, straight from registers, into the owner's shared memory
-//     (st.async, counted on the owner's mbarrier), and the owner adds the
-//     partial sums in rank order -- a fixed order, so the result does not
-//     depend on timing -- and stores the chunk.
+//   * when there are fewer output tiles than SMs, K is split.  The tile's
+//     columns are cut into chunks, each owned by one split; the other splits
+//     hand their partial chunks to the owner -- inside a thread-block
+//     cluster through shared memory (small M; large M without a workspace),
+//     or through a caller workspace in global memory (pairs) -- and the
+//     owner adds the partial sums in split order, a fixed order, so the
+//     result does not depend on timing.
 //
 // With programmatic dependent launch, the first pipeline stages' weight
 // tiles (static data) are fetched before the kernel waits for the previous
@@ -76,6 +82,7 @@ struct GemmArgs {
   int splits;
   int tiles_m, tiles_n, num_tiles;
   int stages;          // pipeline depth
+  int kbs;             // 128-byte k-blocks per pipeline stage (pairs: 2 when K allows)
   int chunk_cols;      // split-K: TMEM columns per chunk (32 large M, 8 small M)
   int recv_in_stages;  // split-K: receive buffers reuse the stage buffers
   int outbuf_off;      // shared-memory layout (bytes from the 1024-aligned base)
@@ -196,6 +203,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   using C = Cfg<kSwap, kPair, kBN>;
   constexpr int kEsize = kFp8 ? 1 : 2;
   const int stages = p.stages;
+  // a stage holds kbs k-blocks: the activation tiles, then the weight tiles
+  const int kbs = kPair ? p.kbs : 1;
+  const uint32_t act_bytes = static_cast<uint32_t>(kbs * C::kActBytes);
+  const uint32_t stage_bytes = static_cast<uint32_t>(kbs * C::kStageBytes);
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte aligned base, by pointer arithmetic on the shared array so
   // that accesses through it stay shared-memory loads and stores
@@ -322,18 +333,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ------------------------------------------------------------ copies
       const uint64_t pol_w = kSwap ? dev::policy_evict_first() : dev::policy_evict_normal();
       const uint64_t pol_a = dev::policy_evict_last();
-      const int total = my_tiles * nkb;
-      // geometry of flat k-block g: tile rows, first weight group, groups, tx bytes
+      const int units = (nkb + kbs - 1) / kbs;  // stages per tile
+      const int total = my_tiles * units;
+      // geometry of flat stage g: tile rows, first weight group, groups, tx bytes
       auto geom = [&](int g, int& tm, int& nbf, int& groups) -> uint32_t {
         int tn;
-        tile_of(g / nkb, tm, tn);
+        tile_of(g / units, tm, tn);
         if constexpr (kPair) {
           // 256-channel tiles: one 128-channel group per CTA; 128-channel
           // tiles: one half group per CTA.  Both CTAs' copies complete on
           // the leader's barrier.
           nbf = kBN == 256 ? 2 * tn + px : tn;
           groups = 1;
-          return static_cast<uint32_t>(2 * C::kStageBytes);
+          return 2u * stage_bytes;  // whole boxes (zero fill counts)
         }
         nbf = kSwap ? tn : tn * (kBN / kTile);
         groups = kSwap ? 1 : min(kBN / kTile, p.nb_total - nbf);
@@ -347,31 +359,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!kPair || leader) dev::mbar_arrive_expect_tx(full0 + 8 * s, tx);
       };
       auto load_weights = [&](int g, int s, int nbf, int groups) {
-        const uint32_t st = sbase + s * C::kStageBytes;
-        const int kb = kb0 + g % nkb;
+        const uint32_t st = sbase + s * stage_bytes;
+        const int kb = kb0 + (g % units) * kbs;
         if constexpr (kPair) {
-          // packed tiles seen as rows of 128 bytes; rows past the weight
-          // (channels >= N) arrive as zeros
+          // packed tiles seen as [tile][128 rows][128 bytes]: one box takes
+          // this CTA's rows of kbs consecutive k-tiles; tiles past the
+          // weight (channels >= N) arrive as zeros
           const int half = kBN == 256 ? 0 : px;
-          dev::tma_load_2d_pair(st + C::kActBytes, &tmap_w, 0,
-                                (nbf * p.kb_total + kb) * kTile + half * (kTile / 2), full_bar(s),
-                                pol_w);
+          dev::tma_load_3d_pair(st + act_bytes, &tmap_w, 0, half * (kTile / 2),
+                                nbf * p.kb_total + kb, full_bar(s), pol_w);
         } else {
           for (int q = 0; q < groups; ++q) {
             const uint8_t* src =
                 p.w_packed + (static_cast<size_t>(nbf + q) * p.kb_total + kb) * kWTile;
-            dev::bulk_load(st + C::kActBytes + q * kWTile, src, kWTile, full0 + 8 * s, pol_w);
+            dev::bulk_load(st + act_bytes + q * kWTile, src, kWTile, full0 + 8 * s, pol_w);
           }
         }
       };
       auto load_act = [&](int g, int s, int tm) {
-        const int x = (kb0 + g % nkb) * (kKBytes / kEsize);
-        if constexpr (kPair)
-          dev::tma_load_2d_pair(sbase + s * C::kStageBytes, &tmap_act, x,
-                                tm * C::kTileRows + px * kTile, full_bar(s), pol_a);
-        else
-          dev::tma_load_2d(sbase + s * C::kStageBytes, &tmap_act, x, tm * C::kActRows,
-                           full0 + 8 * s, pol_a);
+        const int kb = kb0 + (g % units) * kbs;
+        if constexpr (kPair) {
+          // kbs = 2: activations seen as [k-block][row][128 bytes], one box
+          // per stage; kbs = 1: the 2-D view (zero fill past K)
+          if (kbs == 2)
+            dev::tma_load_3d_pair(sbase + s * stage_bytes, &tmap_act, 0,
+                                  tm * C::kTileRows + px * kTile, kb, full_bar(s), pol_a);
+          else
+            dev::tma_load_2d_pair(sbase + s * stage_bytes, &tmap_act, kb * (kKBytes / kEsize),
+                                  tm * C::kTileRows + px * kTile, full_bar(s), pol_a);
+        } else {
+          dev::tma_load_2d(sbase + s * stage_bytes, &tmap_act, kb * (kKBytes / kEsize),
+                           tm * C::kActRows, full0 + 8 * s, pol_a);
+        }
       };
       const int npre = total < stages ? total : stages;
       for (int g = 0; g < npre; ++g) {  // first use of each stage needs no wait
@@ -445,24 +464,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         dev::tc_fence_after();
         const uint32_t d = tmem + static_cast<uint32_t>(b * kBN);
         bool stop = false;
-        for (int i = 0; i < nkb; ++i) {
+        const int units = (nkb + kbs - 1) / kbs;
+        for (int i = 0; i < units; ++i) {
           if (!dev::mbar_wait(full0 + 8 * s, ph & 1, abort_flag, p.dev_status,
                               dev::kTimeoutMma)) {
             stop = true;
             break;
           }
           dev::tc_fence_after();
-          const uint32_t st = sbase + s * C::kStageBytes;
-          const uint32_t a_addr = kSwap ? st + C::kActBytes : st;
-          const uint32_t b_addr = kSwap ? st : st + C::kActBytes;
-          const uint64_t ad = dev::smem_desc_sw128(a_addr);
-          const uint64_t bd = dev::smem_desc_sw128(b_addr);
+          const uint32_t st = sbase + s * stage_bytes;
+          // k-blocks of this stage inside this CTA's K range (a stage past
+          // its end holds another range's or zero data, not multiplied)
+          const int hk = min(kbs, nkb - i * kbs);
+          for (int h = 0; h < hk; ++h) {
+            const uint32_t a_addr = kSwap ? st + act_bytes : st + h * C::kActBytes;
+            const uint32_t b_addr = kSwap ? st : st + act_bytes + h * C::kWBytes;
+            const uint64_t ad = dev::smem_desc_sw128(a_addr);
+            const uint64_t bd = dev::smem_desc_sw128(b_addr);
 #pragma unroll
-          for (int k = 0; k < kKBytes / 32; ++k) {
-            if constexpr (kPair)
-              dev::mma_pair<kFp8>(d, ad + 2 * k, bd + 2 * k, idesc, (i | k) != 0);
-            else
-              dev::mma<kFp8>(d, ad + 2 * k, bd + 2 * k, idesc, (i | k) != 0);
+            for (int k = 0; k < kKBytes / 32; ++k) {
+              if constexpr (kPair)
+                dev::mma_pair<kFp8>(d, ad + 2 * k, bd + 2 * k, idesc, (i | h | k) != 0);
+              else
+                dev::mma<kFp8>(d, ad + 2 * k, bd + 2 * k, idesc, (i | h | k) != 0);
+            }
           }
           commit(empty0 + 8 * s);
           if (++s == stages) {
@@ -872,6 +897,7 @@ struct Plan {
   int kb_per_split;
   int chunk_cols;
   int stages;
+  int kbs;  // k-blocks per stage
   bool recv_in_stages;
   bool split_global;  // split-K through the workspace (CTA pairs)
   size_t ws_bytes;    // workspace the plan uses (split_global), else 0
@@ -974,9 +1000,6 @@ int cluster_capacity_for(const Plan& pl, int s, int smem) {
   if (pl.pair)
     return pl.bn == 128 ? cluster_capacity<kFp8, false, true, 128>(s, smem)
                         : cluster_capacity<kFp8, false, true, 256>(s, smem);
-  if (!pl.swap)
-    return pl.bn == 128 ? cluster_capacity<kFp8, false, false, 128>(s, smem)
-                        : cluster_capacity<kFp8, false, false, 256>(s, smem);
   switch (pl.bn) {
     case 32: return cluster_capacity<kFp8, true, false, 32>(s, smem);
     case 64: return cluster_capacity<kFp8, true, false, 64>(s, smem);
@@ -1061,7 +1084,15 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int esize, bool fp8, size_t ws_a
   const int ctas_per_tile = pl.pair ? 2 : 1;
   const int act_rows = pl.swap ? pl.bn : kTile;
   const int w_rows = pl.swap ? kTile : (pl.pair ? pl.bn / 2 : pl.bn);
-  const int stage_bytes = (act_rows + w_rows) * kKBytes;
+  // pairs: two k-blocks per stage (one box per operand) when K is a whole
+  // number of 128-byte k-blocks, so the activations can be seen as
+  // [k-block][row][128 bytes]
+  pl.kbs = (pl.pair && (K * esize) % kKBytes == 0 && kb >= 2) ? 2 : 1;
+  const int stage_bytes = pl.kbs * (act_rows + w_rows) * kKBytes;
+  // a split's K range is a whole number of stages
+  auto split_kb = [&](int s) {
+    return static_cast<int>(ceil_div(ceil_div(kb, s), pl.kbs) * pl.kbs);
+  };
 
   int s_max = 1, g_max = 1;
   if (pl.num_tiles * ctas_per_tile < sms) {
@@ -1077,7 +1108,7 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int esize, bool fp8, size_t ws_a
   // it and every pair of the grid can be resident at once (the owners of
   // each chunk wait for the other splits' partials)
   for (int s = g_max; s >= 2; --s) {
-    pl.kb_per_split = static_cast<int>(ceil_div(kb, s));
+    pl.kb_per_split = split_kb(s);
     pl.splits = static_cast<int>(ceil_div(kb, pl.kb_per_split));
     if (pl.splits < 2) break;
     pl.split_global = true;
@@ -1092,7 +1123,7 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int esize, bool fp8, size_t ws_a
     pl.ws_bytes = pl.ws_flag_bytes = 0;
   }
   for (int s = pl.split_global ? 0 : s_max; s >= 1; --s) {
-    pl.kb_per_split = static_cast<int>(ceil_div(kb, s));
+    pl.kb_per_split = split_kb(s);
     pl.splits = static_cast<int>(ceil_div(kb, pl.kb_per_split));
     // pipeline depth: small M takes just the CTA's k-blocks (a small
     // footprint lets a dependent grid's CTAs be resident early and
@@ -1157,9 +1188,6 @@ cudaError_t dispatch(const CUtensorMap& ta, const CUtensorMap& tw, const CUtenso
   if (pl.pair)
     return pl.bn == 128 ? launch_one<kFp8, false, true, 128>(ta, tw, to, a, pl, stream)
                         : launch_one<kFp8, false, true, 256>(ta, tw, to, a, pl, stream);
-  if (!pl.swap)
-    return pl.bn == 128 ? launch_one<kFp8, false, false, 128>(ta, tw, to, a, pl, stream)
-                        : launch_one<kFp8, false, false, 256>(ta, tw, to, a, pl, stream);
   switch (pl.bn) {
     case 32: return launch_one<kFp8, true, false, 32>(ta, tw, to, a, pl, stream);
     case 64: return launch_one<kFp8, true, false, 64>(ta, tw, to, a, pl, stream);
@@ -1201,7 +1229,22 @@ frt_status gemm_common(bool fp8, const void* a, int64_t lda, const float* a_scal
   const Plan pl = make_plan(M, N, K, esize, fp8, ws_avail);
 
   CUtensorMap ta, tw, to;
-  {
+  if (pl.pair && pl.kbs == 2) {
+    // activations as [k-block][row][128 bytes of K]; one box = 128 rows of
+    // two consecutive k-blocks (zero fill past M and past the last k-block)
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kKBytes / esize),
+                                static_cast<cuuint64_t>(M), static_cast<cuuint64_t>(kb_total)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(lda * esize),
+                                   static_cast<cuuint64_t>(kKBytes)};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(kKBytes / esize),
+                               static_cast<cuuint32_t>(kTile), 2u};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    if (encode(&ta, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+               const_cast<void*>(a), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return FRT_ERR_CUDA;
+  } else {
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(lda * esize)};
     const cuuint32_t box[2] = {static_cast<cuuint32_t>(kKBytes / esize),
@@ -1214,15 +1257,17 @@ frt_status gemm_common(bool fp8, const void* a, int64_t lda, const float* a_scal
       return FRT_ERR_CUDA;
   }
   if (pl.pair) {
-    // packed weight tiles as rows of 128 bytes (the tiles are stored in
-    // their shared-memory image, so no swizzle); one box = the 128 or 64
-    // channels of one k-block that a pair's CTA holds
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kKBytes),
-                                static_cast<cuuint64_t>(nb_total * kb_total * kTile)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kKBytes)};
-    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kKBytes), static_cast<cuuint32_t>(pl.bn / 2)};
-    const cuuint32_t estr[2] = {1, 1};
-    if (encode(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(w_packed), dims, strides,
+    // packed weight tiles as [tile][128 rows][128 bytes] (the tiles are
+    // stored in their shared-memory image, so no swizzle); one box = the 128
+    // or 64 channels that a pair's CTA holds, of kbs consecutive k-tiles
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kKBytes), static_cast<cuuint64_t>(kTile),
+                                static_cast<cuuint64_t>(nb_total * kb_total)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kKBytes),
+                                   static_cast<cuuint64_t>(kWTile)};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(kKBytes), static_cast<cuuint32_t>(pl.bn / 2),
+                               static_cast<cuuint32_t>(pl.kbs)};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    if (encode(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(w_packed), dims, strides,
                box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return FRT_ERR_CUDA;
@@ -1258,6 +1303,7 @@ frt_status gemm_common(bool fp8, const void* a, int64_t lda, const float* a_scal
   ga.tiles_n = pl.tiles_n;
   ga.num_tiles = pl.num_tiles;
   ga.stages = pl.stages;
+  ga.kbs = pl.kbs;
   ga.chunk_cols = pl.chunk_cols;
   ga.recv_in_stages = pl.recv_in_stages ? 1 : 0;
   ga.outbuf_off = pl.outbuf_off;

@@ -153,14 +153,15 @@ def test_bf16_row_tails(M):
 @pytest.mark.parametrize("M,K,N", [(50, 96, 144), (50, 4096, 1024), (16, 8192, 128),
                                    (300, 16384, 256), (768, 2048, 2560), (130, 96, 16),
                                    (64, 2048, 8192), (1, 4096, 4096), (300, 8192, 384),
-                                   (520, 1024, 4352)])
+                                   (520, 1024, 4352), (300, 1152, 256), (768, 1152, 2560)])
 def test_fp8_shapes_and_splits(M, K, N):
     fp8_layer(rand_layer(M, K, N, seed=K + N))
 
 
 @pytest.mark.parametrize("M,K,N", [(50, 112, 144), (50, 4096, 1024), (16, 8192, 128),
                                    (300, 8192, 256), (768, 2048, 2560), (130, 48, 16),
-                                   (1, 4096, 4096), (300, 8192, 384), (520, 1024, 4352)])
+                                   (1, 4096, 4096), (300, 8192, 384), (520, 1024, 4352),
+                                   (300, 1088, 256), (768, 1088, 2560)])
 def test_bf16_shapes_and_splits(M, K, N):
     bf16_layer(rand_layer(M, K, N, seed=K + N))
 
