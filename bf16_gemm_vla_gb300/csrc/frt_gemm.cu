@@ -204,7 +204,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int kEsize = kFp8 ? 1 : 2;
   const int stages = p.stages;
   // a stage holds kbs k-blocks: the activation tiles, then the weight tiles
-  const int kbs = kPair ? p.kbs : 1;
+  const int kbs = (kPair || kSwap) ? p.kbs : 1;
   const uint32_t act_bytes = static_cast<uint32_t>(kbs * C::kActBytes);
   const uint32_t stage_bytes = static_cast<uint32_t>(kbs * C::kStageBytes);
   extern __shared__ uint8_t smem_raw[];
@@ -347,8 +347,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           groups = 1;
           return 2u * stage_bytes;  // whole boxes (zero fill counts)
         }
-        nbf = kSwap ? tn : tn * (kBN / kTile);
-        groups = kSwap ? 1 : min(kBN / kTile, p.nb_total - nbf);
+        if constexpr (kSwap) {
+          // the channel group's k-tiles of this stage are contiguous; the
+          // copy stops at the group's last k-tile
+          nbf = tn;
+          groups = min(kbs, p.kb_total - (kb0 + (g % units) * kbs));
+          return static_cast<uint32_t>(kbs * C::kActBytes + groups * kWTile);
+        }
+        nbf = tn * (kBN / kTile);
+        groups = min(kBN / kTile, p.nb_total - nbf);
         return static_cast<uint32_t>(C::kActBytes + groups * kWTile);
       };
       // the stage's full barrier: a pair's is the leader's
@@ -368,6 +375,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int half = kBN == 256 ? 0 : px;
           dev::tma_load_3d_pair(st + act_bytes, &tmap_w, 0, half * (kTile / 2),
                                 nbf * p.kb_total + kb, full_bar(s), pol_w);
+        } else if constexpr (kSwap) {
+          const uint8_t* src = p.w_packed + (static_cast<size_t>(nbf) * p.kb_total + kb) * kWTile;
+          dev::bulk_load(st + act_bytes, src, static_cast<uint32_t>(groups * kWTile), full0 + 8 * s,
+                         pol_w);
         } else {
           for (int q = 0; q < groups; ++q) {
             const uint8_t* src =
@@ -387,6 +398,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           else
             dev::tma_load_2d_pair(sbase + s * stage_bytes, &tmap_act, kb * (kKBytes / kEsize),
                                   tm * C::kTileRows + px * kTile, full_bar(s), pol_a);
+        } else if (kbs == 2) {
+          dev::tma_load_3d(sbase + s * stage_bytes, &tmap_act, 0, tm * C::kActRows, kb,
+                           full0 + 8 * s, pol_a);
         } else {
           dev::tma_load_2d(sbase + s * stage_bytes, &tmap_act, kb * (kKBytes / kEsize),
                            tm * C::kActRows, full0 + 8 * s, pol_a);
@@ -477,8 +491,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           // its end holds another range's or zero data, not multiplied)
           const int hk = min(kbs, nkb - i * kbs);
           for (int h = 0; h < hk; ++h) {
-            const uint32_t a_addr = kSwap ? st + act_bytes : st + h * C::kActBytes;
-            const uint32_t b_addr = kSwap ? st : st + act_bytes + h * C::kWBytes;
+            const uint32_t a_addr =
+                kSwap ? st + act_bytes + h * C::kWBytes : st + h * C::kActBytes;
+            const uint32_t b_addr =
+                kSwap ? st + h * C::kActBytes : st + act_bytes + h * C::kWBytes;
             const uint64_t ad = dev::smem_desc_sw128(a_addr);
             const uint64_t bd = dev::smem_desc_sw128(b_addr);
 #pragma unroll
@@ -1087,8 +1103,9 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int esize, bool fp8, size_t ws_a
   // pairs: two k-blocks per stage (one box per operand) when K is a whole
   // number of 128-byte k-blocks, so the activations can be seen as
   // [k-block][row][128 bytes]
-  pl.kbs = (pl.pair && (K * esize) % kKBytes == 0 && kb >= 2) ? 2 : 1;
-  const int stage_bytes = pl.kbs * (act_rows + w_rows) * kKBytes;
+  const bool whole_kb = (K * esize) % kKBytes == 0;
+  pl.kbs = (pl.pair && whole_kb && kb >= 2) ? 2 : 1;
+  int stage_bytes = pl.kbs * (act_rows + w_rows) * kKBytes;
   // a split's K range is a whole number of stages
   auto split_kb = [&](int s) {
     return static_cast<int>(ceil_div(ceil_div(kb, s), pl.kbs) * pl.kbs);
@@ -1123,6 +1140,10 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int esize, bool fp8, size_t ws_a
     pl.ws_bytes = pl.ws_flag_bytes = 0;
   }
   for (int s = pl.split_global ? 0 : s_max; s >= 1; --s) {
+    if (pl.swap) {  // small M: two k-blocks per stage when each CTA has two or more
+      pl.kbs = (whole_kb && ceil_div(kb, s) >= 2) ? 2 : 1;
+      stage_bytes = pl.kbs * (act_rows + w_rows) * kKBytes;
+    }
     pl.kb_per_split = split_kb(s);
     pl.splits = static_cast<int>(ceil_div(kb, pl.kb_per_split));
     // pipeline depth: small M takes just the CTA's k-blocks (a small
@@ -1130,7 +1151,7 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int esize, bool fp8, size_t ws_a
     // prefetch); large M and multi-tile walks take as many as fit
     int want = kMaxStages;
     if (pl.swap) {
-      const int per_cta = pl.splits > 1 ? pl.kb_per_split : kb;
+      const int per_cta = static_cast<int>(ceil_div(pl.splits > 1 ? pl.kb_per_split : kb, pl.kbs));
       want = per_cta < 2 ? 2 : (per_cta > kMaxStages ? kMaxStages : per_cta);
       if (pl.splits == 1 && pl.num_tiles > sms) want = kMaxStages;
     }
@@ -1229,15 +1250,16 @@ frt_status gemm_common(bool fp8, const void* a, int64_t lda, const float* a_scal
   const Plan pl = make_plan(M, N, K, esize, fp8, ws_avail);
 
   CUtensorMap ta, tw, to;
-  if (pl.pair && pl.kbs == 2) {
-    // activations as [k-block][row][128 bytes of K]; one box = 128 rows of
-    // two consecutive k-blocks (zero fill past M and past the last k-block)
+  if (pl.kbs == 2) {
+    // activations as [k-block][row][128 bytes of K]; one box = the CTA's
+    // rows of two consecutive k-blocks (zero fill past M and past the last
+    // k-block)
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kKBytes / esize),
                                 static_cast<cuuint64_t>(M), static_cast<cuuint64_t>(kb_total)};
     const cuuint64_t strides[2] = {static_cast<cuuint64_t>(lda * esize),
                                    static_cast<cuuint64_t>(kKBytes)};
     const cuuint32_t box[3] = {static_cast<cuuint32_t>(kKBytes / esize),
-                               static_cast<cuuint32_t>(kTile), 2u};
+                               static_cast<cuuint32_t>(pl.swap ? pl.bn : kTile), 2u};
     const cuuint32_t estr[3] = {1, 1, 1};
     if (encode(&ta, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
                const_cast<void*>(a), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
