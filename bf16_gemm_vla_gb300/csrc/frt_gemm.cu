@@ -1121,25 +1121,26 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int esize, bool fp8, size_t ws_a
     g_max = pl.pair ? s_max : 1;  // a global split is not bounded by the cluster size
     if (s_max > kMaxSplits / ctas_per_tile) s_max = kMaxSplits / ctas_per_tile;
   }
-  // CTA pairs: split K through the workspace when the caller gave enough of
-  // it and every pair of the grid can be resident at once (the owners of
-  // each chunk wait for the other splits' partials)
-  for (int s = g_max; s >= 2; --s) {
-    pl.kb_per_split = split_kb(s);
-    pl.splits = static_cast<int>(ceil_div(kb, pl.kb_per_split));
-    if (pl.splits < 2) break;
-    pl.split_global = true;
-    global_split_bytes(pl);
-    if (pl.ws_bytes <= ws_avail && place_buffers(pl, stage_bytes, kMaxStages)) {
-      const int smem = pl.smem < kPairMinSmem ? kPairMinSmem : pl.smem;
-      const int capacity = fp8 ? cluster_capacity_for<true>(pl, 1, smem)
-                               : cluster_capacity_for<false>(pl, 1, smem);
-      if (capacity >= pl.num_tiles * pl.splits) break;
+  // CTA pairs: a split of K through the workspace, when the caller gave
+  // enough of it and every pair of the grid can be resident at once (the
+  // owners of each chunk wait for the other splits' partials).  It is taken
+  // below only if it splits K further than a cluster can.
+  Plan gpl = pl;
+  bool have_g = false;
+  for (int s = g_max; s >= 2 && !have_g; --s) {
+    gpl.kb_per_split = split_kb(s);
+    gpl.splits = static_cast<int>(ceil_div(kb, gpl.kb_per_split));
+    if (gpl.splits < 2) break;
+    gpl.split_global = true;
+    global_split_bytes(gpl);
+    if (gpl.ws_bytes <= ws_avail && place_buffers(gpl, stage_bytes, kMaxStages)) {
+      const int smem = gpl.smem < kPairMinSmem ? kPairMinSmem : gpl.smem;
+      const int capacity = fp8 ? cluster_capacity_for<true>(gpl, 1, smem)
+                               : cluster_capacity_for<false>(gpl, 1, smem);
+      have_g = capacity >= gpl.num_tiles * gpl.splits;
     }
-    pl.split_global = false;
-    pl.ws_bytes = pl.ws_flag_bytes = 0;
   }
-  for (int s = pl.split_global ? 0 : s_max; s >= 1; --s) {
+  for (int s = s_max; s >= 1; --s) {
     if (pl.swap) {  // small M: two k-blocks per stage when each CTA has two or more
       pl.kbs = (whole_kb && ceil_div(kb, s) >= 2) ? 2 : 1;
       stage_bytes = pl.kbs * (act_rows + w_rows) * kKBytes;
@@ -1162,6 +1163,9 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int esize, bool fp8, size_t ws_a
                              : cluster_capacity_for<false>(pl, pl.splits, smem);
     if (capacity >= pl.num_tiles) break;
   }
+  // the workspace: deeper splits (no cluster size limit, no cluster
+  // placement); a cluster's shared-memory exchange is cheaper at equal splits
+  if (have_g && gpl.splits > pl.splits) pl = gpl;
   // a pair CTA takes all 512 TMEM columns: with at least kPairMinSmem of
   // shared memory no other GEMM CTA (each takes over 40 KiB) is resident
   // beside it, while the small CTAs of other kernels still are
