@@ -390,15 +390,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto load_act = [&](int g, int s, int tm) {
         const int kb = kb0 + (g % units) * kbs;
         if constexpr (kPair) {
-          // kbs = 2: activations seen as [k-block][row][128 bytes], one box
+          // kbs > 1: activations seen as [k-block][row][128 bytes], one box
           // per stage; kbs = 1: the 2-D view (zero fill past K)
-          if (kbs == 2)
+          if (kbs > 1)
             dev::tma_load_3d_pair(sbase + s * stage_bytes, &tmap_act, 0,
                                   tm * C::kTileRows + px * kTile, kb, full_bar(s), pol_a);
           else
             dev::tma_load_2d_pair(sbase + s * stage_bytes, &tmap_act, kb * (kKBytes / kEsize),
                                   tm * C::kTileRows + px * kTile, full_bar(s), pol_a);
-        } else if (kbs == 2) {
+        } else if (kbs > 1) {
           dev::tma_load_3d(sbase + s * stage_bytes, &tmap_act, 0, tm * C::kActRows, kb,
                            full0 + 8 * s, pol_a);
         } else {
@@ -1100,11 +1100,13 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int esize, bool fp8, size_t ws_a
   const int ctas_per_tile = pl.pair ? 2 : 1;
   const int act_rows = pl.swap ? pl.bn : kTile;
   const int w_rows = pl.swap ? kTile : (pl.pair ? pl.bn / 2 : pl.bn);
-  // pairs: two k-blocks per stage (one box per operand) when K is a whole
-  // number of 128-byte k-blocks, so the activations can be seen as
-  // [k-block][row][128 bytes]
+  // pairs: several k-blocks per stage (one box per operand) when K is a
+  // whole number of 128-byte k-blocks, so the activations can be seen as
+  // [k-block][row][128 bytes]: fewer, larger copies.  Two for 256-channel
+  // tiles (3 stages of 64 KiB), four for 128-channel tiles with 8 or more
+  // k-blocks (2 stages of 96 KiB).
   const bool whole_kb = (K * esize) % kKBytes == 0;
-  pl.kbs = (pl.pair && whole_kb && kb >= 2) ? 2 : 1;
+  pl.kbs = (pl.pair && whole_kb && kb >= 2) ? ((pl.bn == 128 && kb >= 8) ? 4 : 2) : 1;
   int stage_bytes = pl.kbs * (act_rows + w_rows) * kKBytes;
   // a split's K range is a whole number of stages
   auto split_kb = [&](int s) {
@@ -1254,16 +1256,17 @@ frt_status gemm_common(bool fp8, const void* a, int64_t lda, const float* a_scal
   const Plan pl = make_plan(M, N, K, esize, fp8, ws_avail);
 
   CUtensorMap ta, tw, to;
-  if (pl.kbs == 2) {
+  if (pl.kbs > 1) {
     // activations as [k-block][row][128 bytes of K]; one box = the CTA's
-    // rows of two consecutive k-blocks (zero fill past M and past the last
+    // rows of kbs consecutive k-blocks (zero fill past M and past the last
     // k-block)
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kKBytes / esize),
                                 static_cast<cuuint64_t>(M), static_cast<cuuint64_t>(kb_total)};
     const cuuint64_t strides[2] = {static_cast<cuuint64_t>(lda * esize),
                                    static_cast<cuuint64_t>(kKBytes)};
     const cuuint32_t box[3] = {static_cast<cuuint32_t>(kKBytes / esize),
-                               static_cast<cuuint32_t>(pl.swap ? pl.bn : kTile), 2u};
+                               static_cast<cuuint32_t>(pl.swap ? pl.bn : kTile),
+                               static_cast<cuuint32_t>(pl.kbs)};
     const cuuint32_t estr[3] = {1, 1, 1};
     if (encode(&ta, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
                const_cast<void*>(a), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
