@@ -461,6 +461,22 @@ __device__ __forceinline__ float max16(const uint4& w, float m) {
   return m;
 }
 
+// bf16: running max |x| over a 16-byte vector on packed bf16 pairs (sign
+// bits cleared; __hmax2 returns the other operand for a NaN, as fmaxf).
+// The maximum is exact, so the result equals the fp32 path's.
+__device__ __forceinline__ uint32_t max_abs_bf16x8(uint32_t acc, const uint4& w) {
+  __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&acc);
+  const uint32_t ws[4] = {w.x & 0x7FFF7FFFu, w.y & 0x7FFF7FFFu, w.z & 0x7FFF7FFFu,
+                          w.w & 0x7FFF7FFFu};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) a = __hmax2(a, *reinterpret_cast<const __nv_bfloat162*>(&ws[k]));
+  return *reinterpret_cast<const uint32_t*>(&a);
+}
+
+__device__ __forceinline__ float bf16x2_max_to_float(uint32_t acc) {
+  return fmaxf(__uint_as_float(acc << 16), __uint_as_float(acc & 0xFFFF0000u));
+}
+
 // The grid barrier above.  m: this CTA's max |x| (valid in thread 0); g0:
 // the generation read by thread 0 after the dependency wait; red: the block
 // reduction buffer.  Returns s (or NaN if this CTA gave up) in every thread.
@@ -530,8 +546,15 @@ __global__ void __maxnreg__(48) quantize_regs_kernel(
   for (int j = 0; j < kRegVecs; ++j)
     w[j] = v0 + j * stride < n_vec ? __ldcs(xv + v0 + j * stride) : make_uint4(0, 0, 0, 0);
   float m = 0.0f;
+  if constexpr (sizeof(T) == 2) {
+    uint32_t m2 = 0u;
 #pragma unroll
-  for (int j = 0; j < kRegVecs; ++j) m = max16<T>(w[j], m);
+    for (int j = 0; j < kRegVecs; ++j) m2 = max_abs_bf16x8(m2, w[j]);
+    m = bf16x2_max_to_float(m2);
+  } else {
+#pragma unroll
+    for (int j = 0; j < kRegVecs; ++j) m = max16<T>(w[j], m);
+  }
   m = block_max(m, red);
   __syncthreads();  // red is reused by the barrier
   const float sc = grid_scale<kFnuz>(m, g0, hdr, partial, false, red);
@@ -579,13 +602,20 @@ __global__ void __launch_bounds__(kResThreads, 1) quantize_resident_kernel(
   // max |x| of the slice, chunk by chunk as the copies land (NaN is ignored
   // by fmaxf)
   float m = 0.0f;
+  uint32_t m2 = 0u;  // bf16: packed running max
   bool ok = true;
   for (int i = 0; i < nchunks; ++i) {
     ok = dev::mbar_wait(bar0 + 8 * i, 0, nullptr, nullptr, 0) && ok;
     const uint32_t sz = bytes - i * kResChunk < kResChunk ? bytes - i * kResChunk : kResChunk;
-    for (uint32_t v = tid; v < sz / 16; v += kResThreads)
-      m = max16<T>(*reinterpret_cast<const uint4*>(res + i * kResChunk + v * 16), m);
+    for (uint32_t v = tid; v < sz / 16; v += kResThreads) {
+      const uint4 w = *reinterpret_cast<const uint4*>(res + i * kResChunk + v * 16);
+      if constexpr (sizeof(T) == 2)
+        m2 = max_abs_bf16x8(m2, w);
+      else
+        m = max16<T>(w, m);
+    }
   }
+  if constexpr (sizeof(T) == 2) m = bf16x2_max_to_float(m2);
   m = block_max(m, red);
   const bool failed = __syncthreads_or(!ok);  // also: red is reused by the barrier
   const float sc = grid_scale<kFnuz>(m, g0, hdr, partial, failed, red);

@@ -251,3 +251,28 @@ def test_quantize_one_grid_capacity_boundary(extra_row):
     qo, so = quantize.quantize_e4m3(xh, quantize.PER_TENSOR, e4m3.OCP)
     assert s.cpu().numpy()[0] == so
     np.testing.assert_array_equal(q.cpu().numpy(), qo)
+
+
+@pytest.mark.parametrize("rows,cols", [(16, 256), (768, 16384)])
+@pytest.mark.parametrize("case", ["nan", "inf", "subnormal_max"])
+def test_quantize_bf16_amax_specials(rows, cols, case):
+    # per-tensor amax over bf16 input (the one-grid paths, registers and
+    # shared memory): NaNs are ignored, an infinite |x| is the maximum, and
+    # a maximum among bf16 subnormals is exact; bytes and scale match the
+    # oracle bit for bit
+    g = np.random.default_rng(rows + len(case))
+    x = g.standard_normal((rows, cols)) * (1e-39 if case == "subnormal_max" else 1.0)
+    idx = g.integers(0, rows * cols, 64)
+    if case == "nan":
+        x.reshape(-1)[idx] = np.nan
+        x.reshape(-1)[idx[:8]] = -np.nan
+        x.reshape(-1)[idx[8:16]] = -0.0
+    elif case == "inf":
+        x.reshape(-1)[idx[:4]] = -np.inf
+    else:
+        x.reshape(-1)[idx[:4]] = np.nan
+    xd, xh = _dev_input(x, torch.bfloat16)
+    q, s = frt.frt_quantize_e4m3(xd, frt.PER_TENSOR, frt.OCP)
+    qo, so = quantize.quantize_e4m3(xh, quantize.PER_TENSOR, e4m3.OCP)
+    np.testing.assert_array_equal(s.cpu().numpy(), np.float32([so]))
+    np.testing.assert_array_equal(q.cpu().numpy(), qo)
