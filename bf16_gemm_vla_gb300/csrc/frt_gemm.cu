@@ -49,6 +49,8 @@
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 
+#include <cstdio>
+#include <cstring>
 #include <mutex>
 
 #include "frt_device.cuh"
@@ -1385,4 +1387,30 @@ extern "C" frt_status frt_gemm_bf16(const void* a, int64_t lda, const void* w_pa
                                     int* dev_status, frt_stream_t stream) {
   return frt::gemm_common(false, a, lda, nullptr, w_packed, w_scale, bias, M, N, K, act, act_cols,
                           out, ldo, workspace, workspace_bytes, dev_status, stream);
+}
+
+extern "C" int frt_gemm_describe(int64_t M, int64_t N, int64_t K, frt_dtype a_dtype,
+                                 size_t workspace_bytes, char* buf, size_t buf_len) {
+  if (M < 1 || N < 1 || K < 1 || N % 16 != 0) return -1;
+  if (M > (1LL << 31) - 1 || N > (1LL << 31) - 1 || K > (1LL << 31) - 1) return -1;
+  if (a_dtype != FRT_E4M3_OCP && a_dtype != FRT_BF16) return -1;
+  const bool fp8 = a_dtype == FRT_E4M3_OCP;
+  if (K % (fp8 ? 32 : 16) != 0) return -1;
+  const frt::Plan pl = frt::make_plan(M, N, K, fp8 ? 1 : 2, fp8, workspace_bytes);
+  const unsigned cx = pl.pair ? 2u : 1u;
+  const unsigned cz = pl.split_global ? 1u : static_cast<unsigned>(pl.splits);
+  char line[256];
+  const int n = std::snprintf(
+      line, sizeof line,
+      "kind=%s bn=%d kbs=%d stages=%d splits=%d global=%d tiles=%d grid=%u,%u,%u "
+      "cluster=%u,1,%u smem=%d",
+      pl.pair ? "pair" : "swap", pl.bn, pl.kbs, pl.stages, pl.splits, pl.split_global ? 1 : 0,
+      pl.num_tiles, pl.grid.x, pl.grid.y, pl.grid.z, cx, cz, pl.smem);
+  if (n < 0) return -1;
+  if (buf && buf_len > 0) {
+    const size_t c = static_cast<size_t>(n) < buf_len ? static_cast<size_t>(n) : buf_len - 1;
+    std::memcpy(buf, line, c);
+    buf[c] = '\0';
+  }
+  return n;
 }

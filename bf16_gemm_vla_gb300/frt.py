@@ -5,6 +5,8 @@ the library's CUDA kernels; PyTorch provides device memory and the stream.
 Outputs that are not passed in are allocated with torch; for CUDA-graph
 capture pass every buffer in (the calls then allocate nothing).
 """
+import ctypes
+
 import torch
 
 from . import _lib
@@ -177,6 +179,28 @@ def frt_gemm_workspace_bytes(M, N, K, kind="e4m3"):
     device (0: none).  A workspace must be zero-filled before its first use;
     the GEMM leaves it so."""
     return lib().frt_gemm_workspace_bytes(M, N, K, _GEMM_DTYPE[kind])
+
+
+def frt_gemm_describe(M, N, K, kind="e4m3", workspace_bytes=None):
+    """The launch plan of an M x N x K GEMM on the current device, as a dict
+    (kind, bn, kbs, stages, splits, global, tiles, grid, cluster, smem).  workspace_bytes: the usable workspace (None: as much as the plan
+    wants, which is what the default shared workspace provides)."""
+    if workspace_bytes is None:
+        workspace_bytes = (1 << 64) - 1
+    buf = ctypes.create_string_buffer(256)
+    n = lib().frt_gemm_describe(M, N, K, _GEMM_DTYPE[kind], workspace_bytes, buf, len(buf))
+    if n < 0:
+        raise FrtError("frt_gemm_describe: unsupported problem", 1)
+    plan = {}
+    for field in buf.value.decode().split():
+        key, val = field.split("=")
+        if key == "kind":
+            plan[key] = val
+        elif "," in val:
+            plan[key] = tuple(int(v) for v in val.split(","))
+        else:
+            plan[key] = int(val)
+    return plan
 
 
 def gemm_workspace(M, N, K, kind="e4m3", device=None):

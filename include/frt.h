@@ -261,6 +261,25 @@ frt_status frt_pack_weights(const void* w, frt_dtype w_dtype, int64_t K, int64_t
  * ---------------------------------------------------------------------- */
 size_t frt_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, frt_dtype a_dtype);
 
+/* The launch plan frt_gemm_fp8 (a_dtype FRT_E4M3_OCP) or frt_gemm_bf16
+ * (FRT_BF16) takes for an M x N x K problem given a usable workspace of
+ * workspace_bytes bytes, as one line of space-separated key=value fields:
+ *   kind    pair (256-row tiles on CTA pairs) or swap (M <= 128: channels on
+ *           the MMA's M side);
+ *   bn      tile width (channels for pair, rows for swap);
+ *   kbs     128-byte k-blocks per pipeline stage; stages: pipeline depth;
+ *   splits  split-K factor; global: 1 when the split meets in the workspace;
+ *   tiles   output tiles the grid walks;
+ *   grid    X,Y,Z CTAs; cluster: X,Y,Z CTAs; smem: bytes per CTA.
+ * The same shape always gets the same plan (on one device).  Writes at most
+ * buf_len bytes including the terminating NUL (nothing when buf is NULL or
+ * buf_len is 0) and returns the length of the whole line, like snprintf;
+ * returns -1 when the arguments do not describe a supported problem.  Needs
+ * the current CUDA device (the plan depends on its SM count and on how many
+ * clusters fit); launches nothing. */
+int frt_gemm_describe(int64_t M, int64_t N, int64_t K, frt_dtype a_dtype, size_t workspace_bytes,
+                      char* buf, size_t buf_len);
+
 frt_status frt_gemm_fp8(const uint8_t* a_q, int64_t lda, const float* a_scale,
                         const void* w_packed, const float* w_scale, const float* bias,
                         int64_t M, int64_t N, int64_t K, frt_act act, int64_t act_cols,

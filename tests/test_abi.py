@@ -56,6 +56,16 @@ def test_sizes(lib):
     assert lib.frt_gemm_workspace_bytes(50, 1024, 4096, _lib.FRT_E4M3_OCP) == 0
 
 
+def test_gemm_describe_rejects_unsupported_problems(lib):
+    # checked before any device query: N % 16, K % 32 (FP8) / 16 (BF16),
+    # nonpositive sizes and a dtype other than E4M3 OCP or BF16
+    buf = ctypes.create_string_buffer(64)
+    for args in ((50, 1000, 4096, _lib.FRT_E4M3_OCP), (50, 1024, 4080, _lib.FRT_E4M3_OCP),
+                 (50, 1024, 4104, _lib.FRT_BF16), (0, 1024, 4096, _lib.FRT_BF16),
+                 (50, 1024, 4096, _lib.FRT_E4M3_FNUZ)):
+        assert lib.frt_gemm_describe(*args, 0, buf, len(buf)) == -1
+
+
 FAKE = 0x10000  # a 64 KiB-aligned address that is never dereferenced: every
                 # call below fails its host-side checks before any CUDA call
 

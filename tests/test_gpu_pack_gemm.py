@@ -291,3 +291,42 @@ def test_split_k_workspace_bf16():
     y, sumabs = gemm.gemm_bf16(synth.bf16_bits_as_f32(lay["a_bf16"]),
                                obf16.round_to_bf16(lay["w_f32"]), None, lay["bias"], 0)
     assert_gemm_close(o1, y, sumabs, "bf16 workspace split")
+
+
+# ---------------------------------------------------------------- plans
+
+PLAN_SHAPES = [(768, 2048, 2560), (768, 2048, 16384), (768, 16384, 2048), (300, 8192, 384),
+               (520, 1024, 4352), (300, 16384, 256), (768, 1152, 2560), (512, 4096, 4096)]
+
+
+def test_plans_cover_every_pair_kind():
+    # the large-M shapes of the parity tests take every CTA-pair plan kind:
+    # persistent (no split), K split across a cluster, K split through the
+    # workspace; the plan is a pure function of the shape
+    kinds = set()
+    for M, K, N in PLAN_SHAPES:
+        for kind in ("e4m3", "bf16"):
+            pl = frt.frt_gemm_describe(M, N, K, kind)
+            assert pl == frt.frt_gemm_describe(M, N, K, kind)
+            assert pl["kind"] == "pair" and pl["cluster"][0] == 2
+            assert pl["grid"][0] % 2 == 0
+            if pl["global"]:
+                assert pl["cluster"][2] == 1 and pl["grid"][2] == pl["splits"] > 1
+            else:
+                assert pl["cluster"][2] == pl["splits"]
+            kinds.add((pl["global"], pl["splits"] > 1))
+    assert kinds == {(0, False), (0, True), (1, True)}
+    # without a workspace no plan splits through it
+    assert frt.frt_gemm_describe(768, 16384, 2048, "e4m3")["global"] == 1
+    assert frt.frt_gemm_describe(768, 16384, 2048, "e4m3", 0)["global"] == 0
+    small = frt.frt_gemm_describe(50, 1024, 4096, "e4m3")
+    assert small["kind"] == "swap" and small["cluster"][0] == 1
+    with pytest.raises(frt.FrtError):
+        frt.frt_gemm_describe(50, 1000, 4096, "e4m3")  # N % 16 != 0
+
+
+@pytest.mark.parametrize("M,K,N", PLAN_SHAPES)
+def test_plan_shapes_fp8_and_bf16(M, K, N):
+    lay = rand_layer(M, K, N, seed=M + K + N)
+    fp8_layer(lay)
+    bf16_layer(lay)
