@@ -653,6 +653,35 @@ __global__ void __launch_bounds__(kThreads, 1)
                    (static_cast<size_t>((tile * 2 + px) * NC + c) * S + j) * (kTile * 8);
           };
           auto flag = [&](int o) { return p.ws_flag + (tile * 2 + px) * S + o; };
+          // the other splits' partials of this CTA's chunks come into the
+          // stage buffers (idle once the accumulator is complete) by one bulk
+          // copy per (chunk, split), a batch of whole chunks at a time (one
+          // batch unless the splits are many): one wait for all of them
+          const int remote = S - 1;
+          const int per_batch =
+              max(1, (p.stages * stage_bytes) / (remote * static_cast<int>(chunk_bytes)));
+          auto fetch = [&](int c0, bool go) {  // one thread; completes a recv_bar phase
+            if (!go) {
+              dev::mbar_arrive(recv_bar);
+              return;
+            }
+            const int c1 = min(own_c1, c0 + per_batch);
+            const uint64_t pol = dev::policy_evict_first();
+            // the partials were written by other CTAs' generic stores and
+            // acquired through the counter; the copies read them through the
+            // async proxy
+            dev::fence_proxy_async_global();
+            dev::mbar_arrive_expect_tx(recv_bar,
+                                       static_cast<uint32_t>((c1 - c0) * remote) * chunk_bytes);
+            for (int c = c0; c < c1; ++c) {
+              int i = (c - c0) * remote;
+              for (int r = 0; r < S; ++r) {
+                if (r == rank) continue;
+                dev::bulk_load(sbase + static_cast<uint32_t>(i++) * chunk_bytes, slot(c, r),
+                               chunk_bytes, recv_bar, pol);
+              }
+            }
+          };
           // 1. the chunks other splits own -> their slots
           for (int c = 0; c < NC; ++c) {
             if (c >= own_c0 && c < own_c1) continue;
@@ -672,39 +701,54 @@ __global__ void __launch_bounds__(kThreads, 1)
             // 2. wait (bounded) until the other S - 1 splits have written
             //    this CTA's chunks, then return the counter to zero
             if (own_c1 > own_c0) {
-              if (dev::wait_counter(flag(rank), static_cast<unsigned>(S - 1), abort_flag,
-                                    p.dev_status, dev::kTimeoutEpilogue))
+              const bool got = dev::wait_counter(flag(rank), static_cast<unsigned>(S - 1),
+                                                 abort_flag, p.dev_status, dev::kTimeoutEpilogue);
+              if (got)
                 *flag(rank) = 0u;
               else
                 ok = false;
+              fetch(own_c0, got);
             }
           }
           dev::named_sync(1, 128);
           ok = !*abort_flag && ok;
           // 3. own chunks: the S partials added in split order
-          for (int c = own_c0; c < own_c1; ++c) {
-            float acc[32];
-            dev::tmem_ld32(tacc + c * 32, acc);
-            float sum[32];
+          uint32_t rph = 0;
+          for (int c0 = own_c0; c0 < own_c1; c0 += per_batch) {
+            const int c1 = min(own_c1, c0 + per_batch);
+            if (c0 != own_c0) {
+              dev::named_sync(1, 128);  // every thread is done with the previous batch
+              if (et == 0) fetch(c0, !*abort_flag);
+            }
+            // (no abort shortcut: copies in flight land before the CTA exits)
+            ok = dev::mbar_wait(recv_bar, rph, nullptr, p.dev_status, dev::kTimeoutEpilogue) && ok;
+            rph ^= 1u;
+            for (int c = c0; c < c1; ++c) {
+              float acc[32];
+              dev::tmem_ld32(tacc + c * 32, acc);
+              float sum[32];
 #pragma unroll
-            for (int j = 0; j < 32; ++j) sum[j] = 0.0f;
-            for (int r = 0; r < S; ++r) {
-              if (r == rank) {
+              for (int j = 0; j < 32; ++j) sum[j] = 0.0f;
+              const float4* got = reinterpret_cast<const float4*>(
+                  base + static_cast<size_t>((c - c0) * remote) * chunk_bytes);
+              for (int r = 0; r < S; ++r) {
+                if (r == rank) {
 #pragma unroll
-                for (int j = 0; j < 32; ++j) sum[j] += acc[j];
-              } else {
-                const float4* src = slot(c, r);
+                  for (int j = 0; j < 32; ++j) sum[j] += acc[j];
+                } else {
 #pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                  const float4 x = __ldcg(src + q * kTile + row);
-                  sum[4 * q] += x.x;
-                  sum[4 * q + 1] += x.y;
-                  sum[4 * q + 2] += x.z;
-                  sum[4 * q + 3] += x.w;
+                  for (int q = 0; q < 8; ++q) {
+                    const float4 x = got[q * kTile + row];
+                    sum[4 * q] += x.x;
+                    sum[4 * q + 1] += x.y;
+                    sum[4 * q + 2] += x.z;
+                    sum[4 * q + 3] += x.w;
+                  }
+                  got += kTile * 8;  // the next split's chunk
                 }
               }
+              finish32(sum, c * 32, 0);
             }
-            finish32(sum, c * 32, 0);
           }
         }
       } else {
@@ -1137,7 +1181,10 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int esize, bool fp8, size_t ws_a
     if (gpl.splits < 2) break;
     gpl.split_global = true;
     global_split_bytes(gpl);
-    if (gpl.ws_bytes <= ws_avail && place_buffers(gpl, stage_bytes, kMaxStages)) {
+    // (the owners gather the other splits' partials of a chunk into their
+    // stage buffers: at least one chunk's worth must fit)
+    if (gpl.ws_bytes <= ws_avail && place_buffers(gpl, stage_bytes, kMaxStages) &&
+        gpl.stages * stage_bytes >= (gpl.splits - 1) * kTile * gpl.chunk_cols * 4) {
       const int smem = gpl.smem < kPairMinSmem ? kPairMinSmem : gpl.smem;
       const int capacity = fp8 ? cluster_capacity_for<true>(gpl, 1, smem)
                                : cluster_capacity_for<false>(gpl, 1, smem);

@@ -317,8 +317,9 @@ def test_plans_cover_every_pair_kind():
             kinds.add((pl["global"], pl["splits"] > 1))
     assert kinds == {(0, False), (0, True), (1, True)}
     # without a workspace no plan splits through it
-    assert frt.frt_gemm_describe(768, 16384, 2048, "e4m3")["global"] == 1
-    assert frt.frt_gemm_describe(768, 16384, 2048, "e4m3", 0)["global"] == 0
+    M, N, K = 768, 2048, 16384
+    assert frt.frt_gemm_describe(M, N, K, "e4m3")["global"] == 1
+    assert frt.frt_gemm_describe(M, N, K, "e4m3", 0)["global"] == 0
     small = frt.frt_gemm_describe(50, 1024, 4096, "e4m3")
     assert small["kind"] == "swap" and small["cluster"][0] == 1
     with pytest.raises(frt.FrtError):
