@@ -401,18 +401,35 @@ def run_headline(args, device, world, sampler, peaks, peak_kind):
                            "gemm_us_event_separated": statistics.mean(gemm[li]) * 1e6,
                            "quantize_us_event_separated": statistics.mean(quant[li]) * 1e6})
     fp8_peak = peaks["bf16_tflops_sustained"] * FP8_OVER_BF16
-    achieved = tot_flops / tot_time / 1e12
-    traffic = profiled_traffic([(M_ENC, lin.w.K, lin.w.N) for lin in set0.layers])
+    # the dominant kernel: the GEMM instantiation (tile width) with the
+    # largest share of the step's GEMM time, over its launches in one step
+    plans = [frt.frt_gemm_describe(M_ENC, lin.w.N, lin.w.K, "e4m3") for lin in set0.layers]
+    groups = {}
+    for li, pl in enumerate(plans):
+        groups.setdefault((pl["kind"], pl["bn"]), []).append(li)
+    (kind, bn), dom = max(groups.items(), key=lambda kv: sum(gemm_b2b[i] for i in kv[1]))
+    dom_flops = sum(2.0 * M_ENC * set0.layers[i].w.K * set0.layers[i].w.N for i in dom)
+    dom_time = sum(gemm_b2b[i] for i in dom)
+    achieved = dom_flops / dom_time / 1e12
+    traffic = profiled_traffic([(M_ENC, set0.layers[i].w.K, set0.layers[i].w.N) for i in dom])
     roofline = {"bound": "tensor", "achieved": achieved, "peak": fp8_peak, "unit": "TFLOP/s",
                 "frac": achieved / fp8_peak, "traffic": traffic,
-                "traffic_unit": "bytes per launch (mean over the step's 3 GEMM launches, ncu)",
-                "kernel": "gemm_tc_kernel<fp8, CTA-pair 256x128 / 256x256 tiles>",
+                "traffic_unit": "bytes per launch (mean over the kernel's launches in a step, "
+                                "ncu)",
+                "kernel": "gemm_tc_kernel<fp8, %s, %d> (layers %s: %.0f%% of the step's GEMM "
+                          "time)" % (kind, bn, ", ".join("%dx%d" % (set0.layers[i].w.K,
+                                                                    set0.layers[i].w.N)
+                                                        for i in dom),
+                                     100.0 * dom_time / tot_time),
                 "timing": "mean device time per launch, each layer's GEMM launched back to back "
                           "on %d rotating sets (larger than L2) in one CUDA graph, CUDA events "
                           "around the replays on the launching stream" % R,
                 "peak_source": "%s bf16 sustained x %.0f (nominal FP8/BF16 dense ratio), of %s"
                                % (peak_kind, FP8_OVER_BF16, peak_kind),
-                "per_launch_flops": tot_flops / len(set0.layers)}
+                "per_launch_flops": dom_flops / len(dom),
+                "all_gemms": {"achieved": tot_flops / tot_time / 1e12,
+                              "frac": tot_flops / tot_time / 1e12 / fp8_peak,
+                              "launches_per_step": len(set0.layers)}}
 
     # end to end through the public API: every step copies its inputs from
     # pinned host memory, replays its graph and reads its outputs back to

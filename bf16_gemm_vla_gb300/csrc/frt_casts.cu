@@ -374,9 +374,11 @@ __global__ void __launch_bounds__(kQThreads) encode_tensor_kernel(
 // chip.  x is read from memory once.
 //
 // The barrier is sense-reversing: each CTA reads the generation (after the
-// previous grid has completed), stores its maximum among the partials and
-// arrives on the arrival count (acquire-release); the last arrival reduces
-// the partials to s, resets the count and publishes the next generation
+// previous grid has completed), folds its maximum into the header's running
+// maximum (an integer atomic max on the fp32 bits, which orders non-negative
+// floats as their values) and arrives on the arrival count
+// (acquire-release); the last arrival reads the maximum, turns it into s,
+// resets the maximum and the count and publishes the next generation
 // together with s in one 64-bit release store, which the others poll.
 // Waits are bounded; a CTA that gives up records a code in the header's
 // status word and uses s = NaN, so the result is visibly invalid.
@@ -388,7 +390,7 @@ constexpr int kResSmem = kResChunk * kResMaxChunks;
 constexpr int kRegVecs = 3;         // register path: 16-byte vectors per thread
 constexpr int kHeaderFloats = 64;   // workspace header: 256 bytes
 // header words: [0] arrivals, [1] status, [2] generation and [3] scale bits
-// (one 64-bit word)
+// (one 64-bit word), [4] running max |x| (fp32 bits)
 
 __device__ __forceinline__ unsigned long long ld_acquire_gpu_u64(const unsigned* p) {
   unsigned long long v;
@@ -481,45 +483,41 @@ __device__ __forceinline__ float bf16x2_max_to_float(uint32_t acc) {
 // the generation read by thread 0 after the dependency wait; red: the block
 // reduction buffer.  Returns s (or NaN if this CTA gave up) in every thread.
 template <bool kFnuz>
-__device__ __forceinline__ float grid_scale(float m, unsigned g0, unsigned* hdr,
-                                            float* __restrict__ partial, bool failed, float* red) {
+__device__ __forceinline__ float grid_scale(float m, unsigned g0, unsigned* hdr, bool failed) {
   __shared__ float s_sh;
-  __shared__ int last_sh, fail_sh;
   if (threadIdx.x == 0) {
-    fail_sh = failed;
-    partial[blockIdx.x] = m;  // ordered before the arrival by its release
-    last_sh = atom_add_acq_rel_gpu(hdr, 1u) == gridDim.x - 1;
-  }
-  __syncthreads();
-  if (last_sh) {
-    float a = 0.0f;
-    for (int i = threadIdx.x; i < static_cast<int>(gridDim.x); i += blockDim.x)
-      a = fmaxf(a, __ldcg(partial + i));
-    a = block_max(a, red);
-    if (threadIdx.x == 0) {
-      const float sc = a == 0.0f ? 1.0f : __fdiv_rn(a, kFnuz ? 240.0f : 448.0f);
+    bool fail = failed;
+    float sc;
+    // m >= 0 and never NaN (fmaxf from 0): its bits order as its value.  The
+    // max is ordered before the arrival by the arrival's release.
+    atomicMax(hdr + 4, __float_as_uint(m));
+    if (atom_add_acq_rel_gpu(hdr, 1u) == gridDim.x - 1) {
+      // every other CTA's max was released before its arrival
+      const float a = __uint_as_float(dev::ld_acquire_gpu(hdr + 4));
+      sc = a == 0.0f ? 1.0f : __fdiv_rn(a, kFnuz ? 240.0f : 448.0f);
+      hdr[4] = 0u;
       hdr[0] = 0u;
       st_release_gpu_u64(hdr + 2, static_cast<unsigned long long>(g0 + 1u) |
                                       (static_cast<unsigned long long>(__float_as_uint(sc)) << 32));
-      s_sh = sc;
-    }
-  } else if (threadIdx.x == 0) {
-    const uint64_t t0 = dev::globaltimer_ns();
-    for (uint32_t it = 0;; ++it) {
-      const unsigned long long w = ld_acquire_gpu_u64(hdr + 2);
-      if (static_cast<unsigned>(w) != g0) {
-        s_sh = __uint_as_float(static_cast<unsigned>(w >> 32));
-        break;
+    } else {
+      const uint64_t t0 = dev::globaltimer_ns();
+      for (uint32_t it = 0;; ++it) {
+        const unsigned long long w = ld_acquire_gpu_u64(hdr + 2);
+        if (static_cast<unsigned>(w) != g0) {
+          sc = __uint_as_float(static_cast<unsigned>(w >> 32));
+          break;
+        }
+        if ((it & 15u) == 15u && dev::globaltimer_ns() - t0 > dev::kWaitLimitNs) {
+          fail = true;
+          break;
+        }
       }
-      if ((it & 15u) == 15u && dev::globaltimer_ns() - t0 > dev::kWaitLimitNs) {
-        fail_sh = 1;
-        break;
-      }
     }
-  }
-  if (threadIdx.x == 0 && fail_sh) {
-    s_sh = __uint_as_float(0x7FC00000u);
-    atomicCAS(hdr + 1, 0u, 0x201u);
+    if (fail) {
+      sc = __uint_as_float(0x7FC00000u);
+      atomicCAS(hdr + 1, 0u, 0x201u);
+    }
+    s_sh = sc;
   }
   __syncthreads();
   return s_sh;
@@ -532,7 +530,7 @@ __device__ __forceinline__ float grid_scale(float m, unsigned g0, unsigned* hdr,
 template <typename T, bool kFnuz>
 __global__ void __maxnreg__(48) quantize_regs_kernel(
     const T* __restrict__ x, int64_t n_vec, uint8_t* __restrict__ q, float* __restrict__ scale_out,
-    unsigned* __restrict__ hdr, float* __restrict__ partial) {
+    unsigned* __restrict__ hdr) {
   constexpr int VEC = 16 / sizeof(T);
   __shared__ float red[32];
   dev::grid_launch_dependents();
@@ -556,8 +554,7 @@ __global__ void __maxnreg__(48) quantize_regs_kernel(
     for (int j = 0; j < kRegVecs; ++j) m = max16<T>(w[j], m);
   }
   m = block_max(m, red);
-  __syncthreads();  // red is reused by the barrier
-  const float sc = grid_scale<kFnuz>(m, g0, hdr, partial, false, red);
+  const float sc = grid_scale<kFnuz>(m, g0, hdr, false);
   if (blockIdx.x == 0 && threadIdx.x == 0 && scale_out) *scale_out = sc;
   const float r = __frcp_rn(sc);
   const bool fast_ok = recip_is_normal(sc, r);
@@ -570,7 +567,7 @@ __global__ void __maxnreg__(48) quantize_regs_kernel(
 template <typename T, bool kFnuz>
 __global__ void __launch_bounds__(kResThreads, 1) quantize_resident_kernel(
     const T* __restrict__ x, int64_t n, int64_t per_cta, uint8_t* __restrict__ q,
-    float* __restrict__ scale_out, unsigned* __restrict__ hdr, float* __restrict__ partial) {
+    float* __restrict__ scale_out, unsigned* __restrict__ hdr) {
   constexpr int VEC = 16 / sizeof(T);
   extern __shared__ __align__(128) uint8_t res[];
   __shared__ uint64_t bars[kResMaxChunks];
@@ -617,8 +614,8 @@ __global__ void __launch_bounds__(kResThreads, 1) quantize_resident_kernel(
   }
   if constexpr (sizeof(T) == 2) m = bf16x2_max_to_float(m2);
   m = block_max(m, red);
-  const bool failed = __syncthreads_or(!ok);  // also: red is reused by the barrier
-  const float sc = grid_scale<kFnuz>(m, g0, hdr, partial, failed, red);
+  const bool failed = __syncthreads_or(!ok);
+  const float sc = grid_scale<kFnuz>(m, g0, hdr, failed);
   dev::grid_launch_dependents();  // every CTA is past the barrier
   if (blockIdx.x == 0 && tid == 0 && scale_out) *scale_out = sc;
   const float r = __frcp_rn(sc);
@@ -729,8 +726,8 @@ frt_status quantize_typed(const T* x, int64_t rows, int64_t cols, int64_t ldx, f
       attr[0].val.programmaticStreamSerializationAllowed = 1;
       cfg.attrs = attr;
       cfg.numAttrs = 1;
-      if (cudaLaunchKernelEx(&cfg, quantize_regs_kernel<T, kFnuz>, x, n_vec16, q, scale, hdr,
-                             ws) != cudaSuccess) {
+      if (cudaLaunchKernelEx(&cfg, quantize_regs_kernel<T, kFnuz>, x, n_vec16, q, scale,
+                             hdr) != cudaSuccess) {
         cudaGetLastError();
         return FRT_ERR_CUDA;
       }
@@ -758,8 +755,8 @@ frt_status quantize_typed(const T* x, int64_t rows, int64_t cols, int64_t ldx, f
       attr[0].val.programmaticStreamSerializationAllowed = 1;
       cfg.attrs = attr;
       cfg.numAttrs = 1;
-      if (cudaLaunchKernelEx(&cfg, quantize_resident_kernel<T, kFnuz>, x, n, per, q, scale, hdr,
-                             ws) != cudaSuccess) {
+      if (cudaLaunchKernelEx(&cfg, quantize_resident_kernel<T, kFnuz>, x, n, per, q, scale,
+                             hdr) != cudaSuccess) {
         cudaGetLastError();
         return FRT_ERR_CUDA;
       }

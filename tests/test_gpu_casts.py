@@ -216,7 +216,9 @@ def test_quantize_workspace_reused_across_shapes():
     # one zero-filled workspace through a sequence of per-tensor shapes whose
     # one-grid launches have different CTA counts (and a strided view, which
     # takes the two-kernel path): every result is the oracle's and the
-    # header (arrivals, status) is back at zero
+    # header (arrivals, status, running maximum) is back at zero; the inputs'
+    # maxima go down as well as up, so a maximum left over from a call would
+    # show in the next scale
     nb = frt.frt_quantize_workspace_bytes(768, 16384, frt.PER_TENSOR)
     ws = torch.zeros((nb // 4,), dtype=torch.float32, device="cuda")
     g = np.random.default_rng(21)
@@ -234,8 +236,8 @@ def test_quantize_workspace_reused_across_shapes():
         qo, so = quantize.quantize_e4m3(xh, quantize.PER_TENSOR, e4m3.OCP)
         assert s.cpu().numpy()[0] == so
         np.testing.assert_array_equal(q.cpu().numpy(), qo)
-        hdr = ws[:4].view(torch.int32).cpu().numpy()
-        assert hdr[0] == 0 and hdr[1] == 0  # arrivals, status
+        hdr = ws[:8].view(torch.int32).cpu().numpy()
+        assert hdr[0] == 0 and hdr[1] == 0 and hdr[4] == 0  # arrivals, status, maximum
 
 
 @pytest.mark.parametrize("extra_row", [0, 1])
