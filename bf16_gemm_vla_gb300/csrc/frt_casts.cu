@@ -379,7 +379,7 @@ __global__ void __launch_bounds__(kQThreads) encode_tensor_kernel(
 // floats as their values) and arrives on the arrival count
 // (acquire-release); the last arrival reads the maximum, turns it into s,
 // resets the maximum and the count and publishes the next generation
-// together with s in one 64-bit release store, which the others poll.
+// together with s in one 64-bit store, which the others poll.
 // Waits are bounded; a CTA that gives up records a code in the header's
 // status word and uses s = NaN, so the result is visibly invalid.
 constexpr int kResThreads = 1024;   // shared-memory path
@@ -392,14 +392,20 @@ constexpr int kHeaderFloats = 64;   // workspace header: 256 bytes
 // header words: [0] arrivals, [1] status, [2] generation and [3] scale bits
 // (one 64-bit word), [4] running max |x| (fp32 bits)
 
-__device__ __forceinline__ unsigned long long ld_acquire_gpu_u64(const unsigned* p) {
+__device__ __forceinline__ unsigned long long ld_relaxed_gpu_u64(const unsigned* p) {
   unsigned long long v;
-  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
   return v;
 }
 
-__device__ __forceinline__ void st_release_gpu_u64(unsigned* p, unsigned long long v) {
-  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+__device__ __forceinline__ unsigned ld_relaxed_gpu(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_relaxed_gpu_u64(unsigned* p, unsigned long long v) {
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
 __device__ __forceinline__ unsigned atom_add_acq_rel_gpu(unsigned* p, unsigned v) {
@@ -492,17 +498,21 @@ __device__ __forceinline__ float grid_scale(float m, unsigned g0, unsigned* hdr,
     // max is ordered before the arrival by the arrival's release.
     atomicMax(hdr + 4, __float_as_uint(m));
     if (atom_add_acq_rel_gpu(hdr, 1u) == gridDim.x - 1) {
-      // every other CTA's max was released before its arrival
-      const float a = __uint_as_float(dev::ld_acquire_gpu(hdr + 4));
+      // every other CTA's max was released before its arrival, and this
+      // arrival's acquire orders the load after them
+      const float a = __uint_as_float(ld_relaxed_gpu(hdr + 4));
       sc = a == 0.0f ? 1.0f : __fdiv_rn(a, kFnuz ? 240.0f : 448.0f);
+      // the resets reach memory before the next grid starts (grid
+      // completion); the waiters read nothing but the published word, so
+      // none of these stores needs ordering
       hdr[4] = 0u;
       hdr[0] = 0u;
-      st_release_gpu_u64(hdr + 2, static_cast<unsigned long long>(g0 + 1u) |
+      st_relaxed_gpu_u64(hdr + 2, static_cast<unsigned long long>(g0 + 1u) |
                                       (static_cast<unsigned long long>(__float_as_uint(sc)) << 32));
     } else {
       const uint64_t t0 = dev::globaltimer_ns();
       for (uint32_t it = 0;; ++it) {
-        const unsigned long long w = ld_acquire_gpu_u64(hdr + 2);
+        const unsigned long long w = ld_relaxed_gpu_u64(hdr + 2);
         if (static_cast<unsigned>(w) != g0) {
           sc = __uint_as_float(static_cast<unsigned>(w >> 32));
           break;
@@ -535,7 +545,8 @@ __global__ void __maxnreg__(48) quantize_regs_kernel(
   __shared__ float red[32];
   dev::grid_launch_dependents();
   dev::grid_dependency_wait();  // x may come from the previous grid
-  const unsigned g0 = threadIdx.x == 0 ? dev::ld_acquire_gpu(hdr + 2) : 0u;
+  // (the previous grid is complete: its header words are visible)
+  const unsigned g0 = threadIdx.x == 0 ? ld_relaxed_gpu(hdr + 2) : 0u;
   const uint4* xv = reinterpret_cast<const uint4*>(x);
   const int64_t stride = static_cast<int64_t>(gridDim.x) * kRegThreads;
   const int64_t v0 = static_cast<int64_t>(blockIdx.x) * kRegThreads + threadIdx.x;
@@ -586,7 +597,7 @@ __global__ void __launch_bounds__(kResThreads, 1) quantize_resident_kernel(
   dev::grid_dependency_wait();  // x may come from the previous grid
   unsigned g0 = 0;
   if (tid == 0) {
-    g0 = dev::ld_acquire_gpu(hdr + 2);
+    g0 = ld_relaxed_gpu(hdr + 2);  // the previous grid is complete
     const uint64_t pol = dev::policy_evict_first();
     const uint8_t* src = reinterpret_cast<const uint8_t*>(x + e0);
     for (int i = 0; i < nchunks; ++i) {
