@@ -197,14 +197,8 @@ __device__ __forceinline__ uint32_t chunk_off(int r, int q, int cw) {
   return static_cast<uint32_t>(r * cw * 4 + ((q ^ swz) << 4));
 }
 
-// At most kMaxRegs registers a thread: a GEMM CTA (256 x 144) then fits
-// beside a register-path quantize CTA (512 x 48) in one SM's register file,
-// so the GEMM grid that follows a quantize becomes resident while the
-// quantize runs (programmatic dependent launch) and prefetches its weights.
-constexpr int kMaxRegs = 144;
-
 template <bool kFp8, bool kSwap, bool kPair, int kBN>
-__global__ void __maxnreg__(kMaxRegs)
+__global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_act,
                    const __grid_constant__ CUtensorMap tmap_w,
                    const __grid_constant__ CUtensorMap tmap_out, const GemmArgs p) {
@@ -632,7 +626,7 @@ __global__ void __maxnreg__(kMaxRegs)
       };
 
       if (!split) {
-        if constexpr (kBN >= 64 && !kPair) {
+        if constexpr (kBN >= 64) {
 #pragma unroll 1
           for (int c = 0; c < kBN; c += 64) {
             float v[64];
@@ -641,15 +635,6 @@ __global__ void __maxnreg__(kMaxRegs)
             if (c + 64 == kBN && it + 1 < my_tiles) release_acc(b);
             finish32(v, c, tm * kBN);
             finish32(v + 32, c + 32, tm * kBN);
-          }
-        } else if constexpr (kPair) {
-          // 32 columns at a time: fewer live registers (kMaxRegs)
-#pragma unroll 1
-          for (int c = 0; c < kBN; c += 32) {
-            float v[32];
-            dev::tmem_ld32(tacc + c, v);
-            if (c + 32 == kBN && it + 1 < my_tiles) release_acc(b);
-            finish32(v, c, tm * kBN);
           }
         } else {
           float v[32];
