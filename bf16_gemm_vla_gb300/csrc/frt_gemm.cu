@@ -221,8 +221,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tfull0 = empty0 + 8 * stages;
   const uint32_t tempty0 = tfull0 + 16;
   const uint32_t recv_bar = tempty0 + 16;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * stages + 5);
+  const uint32_t scale_bar = recv_bar + 8;  // the activation scale is in a_scale_s
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * stages + 6);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float* a_scale_s = reinterpret_cast<float*>(tmem_slot + 2);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -273,6 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     dev::mbar_init(tempty0, kPair ? 8 : 4);
     dev::mbar_init(tempty0 + 8, kPair ? 8 : 4);
     dev::mbar_init(recv_bar, 1);
+    dev::mbar_init(scale_bar, 1);
     *abort_flag = 0;
     dev::fence_mbar_init();
     if (csplit)  // bytes this CTA receives: its own chunks from every peer
@@ -337,10 +340,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t pol_a = dev::policy_evict_last();
       const int units = (nkb + kbs - 1) / kbs;  // stages per tile
       const int total = my_tiles * units;
-      // geometry of flat stage g: tile rows, first weight group, groups, tx bytes
-      auto geom = [&](int g, int& tm, int& nbf, int& groups) -> uint32_t {
-        int tn;
-        tile_of(g / units, tm, tn);
+      // stage cursor: the walk's tile as (x, y), x the fastest coordinate of
+      // tile_of, and the stage i within it; advanced without divisions (the
+      // copy issue is on the critical path while the pipeline fills)
+      struct Cur {
+        int i, x, y;
+      };
+      const int inner = kSwap ? p.tiles_n : p.tiles_m;
+      const int step_q = t_step / inner, step_r = t_step % inner;
+      const Cur start = {0, first_tile % inner, first_tile / inner};
+      auto advance = [&](Cur& c) {
+        if (++c.i == units) {
+          c.i = 0;
+          c.x += step_r;
+          c.y += step_q;
+          if (c.x >= inner) {
+            c.x -= inner;
+            ++c.y;
+          }
+        }
+      };
+      // geometry of a stage: tile rows, first weight group, groups, tx bytes
+      auto geom = [&](const Cur& c, int& tm, int& nbf, int& groups) -> uint32_t {
+        tm = kSwap ? c.y : c.x;
+        const int tn = kSwap ? c.x : c.y;
         if constexpr (kPair) {
           // 256-channel tiles: one 128-channel group per CTA; 128-channel
           // tiles: one half group per CTA.  Both CTAs' copies complete on
@@ -353,7 +376,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // the channel group's k-tiles of this stage are contiguous; the
           // copy stops at the group's last k-tile
           nbf = tn;
-          groups = min(kbs, p.kb_total - (kb0 + (g % units) * kbs));
+          groups = min(kbs, p.kb_total - (kb0 + c.i * kbs));
           return static_cast<uint32_t>(kbs * C::kActBytes + groups * kWTile);
         }
         nbf = tn * (kBN / kTile);
@@ -367,9 +390,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto arm = [&](int s, uint32_t tx) {
         if (!kPair || leader) dev::mbar_arrive_expect_tx(full0 + 8 * s, tx);
       };
-      auto load_weights = [&](int g, int s, int nbf, int groups) {
+      auto load_weights = [&](const Cur& c, int s, int nbf, int groups) {
         const uint32_t st = sbase + s * stage_bytes;
-        const int kb = kb0 + (g % units) * kbs;
+        const int kb = kb0 + c.i * kbs;
         if constexpr (kPair) {
           // packed tiles seen as [tile][128 rows][128 bytes]: one box takes
           // this CTA's rows of kbs consecutive k-tiles; tiles past the
@@ -389,8 +412,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       };
-      auto load_act = [&](int g, int s, int tm) {
-        const int kb = kb0 + (g % units) * kbs;
+      auto load_act = [&](const Cur& c, int s, int tm) {
+        const int kb = kb0 + c.i * kbs;
         if constexpr (kPair) {
           // kbs > 1: activations seen as [k-block][row][128 bytes], one box
           // per stage; kbs = 1: the 2-D view (zero fill past K)
@@ -409,18 +432,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       };
       const int npre = total < stages ? total : stages;
+      Cur cur = start;
       for (int g = 0; g < npre; ++g) {  // first use of each stage needs no wait
         int tm, nbf, groups;
-        const uint32_t tx = geom(g, tm, nbf, groups);
+        const uint32_t tx = geom(cur, tm, nbf, groups);
         arm(g, tx);
-        load_weights(g, g, nbf, groups);
+        load_weights(cur, g, nbf, groups);
+        advance(cur);
       }
       dev::grid_dependency_wait();
+      cur = start;
       for (int g = 0; g < npre; ++g) {
         int tm, nbf, groups;
-        geom(g, tm, nbf, groups);
-        load_act(g, g, tm);
+        geom(cur, tm, nbf, groups);
+        load_act(cur, g, tm);
+        advance(cur);
       }
+      // the activation scale comes from the previous grid: fetched here
+      // (after the dependency wait, through L2) while the first stages land,
+      // and handed to the epilogue through shared memory (the arrival
+      // releases the store, the epilogue's wait acquires it)
+      *a_scale_s = p.a_scale ? __ldcg(p.a_scale) : 1.0f;
+      dev::mbar_arrive(scale_bar);
       int issued = npre;
       int s = npre % stages;
       uint32_t ph = static_cast<uint32_t>(npre / stages);
@@ -429,10 +462,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                             dev::kTimeoutProducer))
           break;
         int tm, nbf, groups;
-        const uint32_t tx = geom(g, tm, nbf, groups);
+        const uint32_t tx = geom(cur, tm, nbf, groups);
         arm(s, tx);
-        load_weights(g, s, nbf, groups);
-        load_act(g, s, tm);
+        load_weights(cur, s, nbf, groups);
+        load_act(cur, s, tm);
+        advance(cur);
         issued = g + 1;
         if (++s == stages) {
           s = 0;
@@ -557,8 +591,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         wsc[j] = n < p.N ? (p.w_scale ? __ldg(p.w_scale + n) : 1.0f) : 0.0f;
         wbi[j] = (n < p.N && p.bias) ? __ldg(p.bias + n) : 0.0f;
       }
+      // the activation scale from the copy thread (waited once, bounded),
+      // then the accumulator
+      const bool scale_ok =
+          it != 0 || dev::mbar_wait(scale_bar, 0, abort_flag, p.dev_status, dev::kTimeoutEpilogue);
       ok = dev::mbar_wait(tfull0 + 8 * b, u & 1, abort_flag, p.dev_status,
-                          dev::kTimeoutEpilogue);
+                          dev::kTimeoutEpilogue) &&
+           scale_ok;
       ok = __all_sync(0xffffffffu, ok);
       if (early_bye && it + 1 == my_tiles) {
         dev::cluster_arrive_relaxed();
@@ -566,10 +605,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       dev::tc_fence_after();
       const uint32_t tacc = tmem + lane_off + static_cast<uint32_t>(b * kBN);
-      // the activation scale comes from the previous grid: read it only now
-      // (after the MMAs consumed activations loaded after the dependency
-      // wait) and through L2
-      const float as = p.a_scale ? __ldcg(p.a_scale) : 1.0f;
+      const float as = *a_scale_s;  // from the copy thread (scale_bar, waited above)
       float* cs_s = col_sb + (it & 1) * 2 * kBN;  // per-channel scale and bias of the tile
       float* cb_s = cs_s + kBN;
       float lcs = 1.0f, lcb = 0.0f;
