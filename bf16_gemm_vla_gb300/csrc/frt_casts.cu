@@ -153,13 +153,35 @@ __device__ __forceinline__ uint32_t cvt_e4m3x2_ocp(float lo, float hi) {
   return r;
 }
 
+// Two fp32 lanes in one 64-bit register, and their lane-wise products (each
+// lane an IEEE round-to-nearest multiply, as the scalar one).
+__device__ __forceinline__ unsigned long long f32x2(float lo, float hi) {
+  unsigned long long d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
+  return d;
+}
+
+__device__ __forceinline__ unsigned long long mul_f32x2(unsigned long long a,
+                                                        unsigned long long b) {
+  unsigned long long d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t cvt_e4m3x2_ocp(unsigned long long v) {
+  float lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+  return cvt_e4m3x2_ocp(lo, hi);
+}
+
 __device__ __forceinline__ uint32_t quantize_pair_ocp(float a, float b, float s, float r,
                                                       bool fast_ok) {
   if (fast_ok) {
-    const float ya = a * r, yb = b * r;
+    // the pair's products and both brackets on packed lanes
+    const unsigned long long y = mul_f32x2(f32x2(a, b), f32x2(r, r));
     const float kDown = 1.0f - 0x1p-20f, kUp = 1.0f + 0x1p-20f;
-    const uint32_t c0 = cvt_e4m3x2_ocp(ya * kDown, yb * kDown);
-    const uint32_t c1 = cvt_e4m3x2_ocp(ya * kUp, yb * kUp);
+    const uint32_t c0 = cvt_e4m3x2_ocp(mul_f32x2(y, f32x2(kDown, kDown)));
+    const uint32_t c1 = cvt_e4m3x2_ocp(mul_f32x2(y, f32x2(kUp, kUp)));
     if (c0 == c1) return c0;
     uint32_t out = 0;
     out |= ((c0 ^ c1) & 0x00FFu) ? encode_e4m3<false>(__fdiv_rn(a, s)) : (c0 & 0x00FFu);
