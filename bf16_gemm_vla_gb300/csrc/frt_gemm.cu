@@ -591,26 +591,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         wsc[j] = n < p.N ? (p.w_scale ? __ldg(p.w_scale + n) : 1.0f) : 0.0f;
         wbi[j] = (n < p.N && p.bias) ? __ldg(p.bias + n) : 0.0f;
       }
-      // the activation scale from the copy thread (waited once, bounded),
-      // then the accumulator
+      // the activation scale from the copy thread (waited once, bounded);
+      // the tile's per-channel factors are staged before its accumulator is
+      // waited for
       const bool scale_ok =
           it != 0 || dev::mbar_wait(scale_bar, 0, abort_flag, p.dev_status, dev::kTimeoutEpilogue);
-      ok = dev::mbar_wait(tfull0 + 8 * b, u & 1, abort_flag, p.dev_status,
-                          dev::kTimeoutEpilogue) &&
-           scale_ok;
-      ok = __all_sync(0xffffffffu, ok);
-      if (early_bye && it + 1 == my_tiles) {
-        dev::cluster_arrive_relaxed();
-        bye = true;
-      }
-      dev::tc_fence_after();
-      const uint32_t tacc = tmem + lane_off + static_cast<uint32_t>(b * kBN);
-      const float as = *a_scale_s;  // from the copy thread (scale_bar, waited above)
+      const float as = *a_scale_s;
       float* cs_s = col_sb + (it & 1) * 2 * kBN;  // per-channel scale and bias of the tile
       float* cb_s = cs_s + kBN;
       float lcs = 1.0f, lcb = 0.0f;
       bool lact = false;
       if constexpr (!kSwap) {
+        // (the buffer was last read in tile it - 2: every warp has passed
+        // tile it - 1's barrier below since)
 #pragma unroll
         for (int j = 0; j < kColsPerThread; ++j) {
           cs_s[et + 128 * j] = as * wsc[j];
@@ -625,6 +618,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           lact = n < p.act_cols;
         }
       }
+      ok = dev::mbar_wait(tfull0 + 8 * b, u & 1, abort_flag, p.dev_status,
+                          dev::kTimeoutEpilogue) &&
+           scale_ok;
+      ok = __all_sync(0xffffffffu, ok);
+      if (early_bye && it + 1 == my_tiles) {
+        dev::cluster_arrive_relaxed();
+        bye = true;
+      }
+      dev::tc_fence_after();
+      const uint32_t tacc = tmem + lane_off + static_cast<uint32_t>(b * kBN);
       const int row0 = tm * C::kTileRows + px * kTile;  // large M: first output row of this CTA
       // epilogue of 32 accumulator columns starting at tile column c32, and
       // this warp's store of them
