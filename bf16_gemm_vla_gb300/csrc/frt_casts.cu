@@ -559,16 +559,19 @@ __device__ __forceinline__ float grid_scale(float m, unsigned g0, unsigned* hdr,
 // A CTA takes at most 512 x 48 registers and no shared memory, so a GEMM CTA
 // (the usual next grid) fits beside it: the next grid is let go at once,
 // and its prologue and weight prefetch overlap this grid.
+//
+// With a static scale (calibrated, frozen) there is no amax and no barrier:
+// each CTA encodes its part as soon as it holds it, and no header is used.
 template <typename T, bool kFnuz>
 __global__ void __maxnreg__(48) quantize_regs_kernel(
     const T* __restrict__ x, int64_t n_vec, uint8_t* __restrict__ q, float* __restrict__ scale_out,
-    unsigned* __restrict__ hdr) {
+    unsigned* __restrict__ hdr, const float* __restrict__ static_scale) {
   constexpr int VEC = 16 / sizeof(T);
   __shared__ float red[32];
   dev::grid_launch_dependents();
-  dev::grid_dependency_wait();  // x may come from the previous grid
+  dev::grid_dependency_wait();  // x (and a static scale) may come from the previous grid
   // (the previous grid is complete: its header words are visible)
-  const unsigned g0 = threadIdx.x == 0 ? ld_relaxed_gpu(hdr + 2) : 0u;
+  const unsigned g0 = (!static_scale && threadIdx.x == 0) ? ld_relaxed_gpu(hdr + 2) : 0u;
   const uint4* xv = reinterpret_cast<const uint4*>(x);
   const int64_t stride = static_cast<int64_t>(gridDim.x) * kRegThreads;
   const int64_t v0 = static_cast<int64_t>(blockIdx.x) * kRegThreads + threadIdx.x;
@@ -576,18 +579,23 @@ __global__ void __maxnreg__(48) quantize_regs_kernel(
 #pragma unroll
   for (int j = 0; j < kRegVecs; ++j)
     w[j] = v0 + j * stride < n_vec ? __ldcs(xv + v0 + j * stride) : make_uint4(0, 0, 0, 0);
-  float m = 0.0f;
-  if constexpr (sizeof(T) == 2) {
-    uint32_t m2 = 0u;
-#pragma unroll
-    for (int j = 0; j < kRegVecs; ++j) m2 = max_abs_bf16x8(m2, w[j]);
-    m = bf16x2_max_to_float(m2);
+  float sc;
+  if (static_scale) {
+    sc = __ldg(static_scale);
   } else {
+    float m = 0.0f;
+    if constexpr (sizeof(T) == 2) {
+      uint32_t m2 = 0u;
 #pragma unroll
-    for (int j = 0; j < kRegVecs; ++j) m = max16<T>(w[j], m);
+      for (int j = 0; j < kRegVecs; ++j) m2 = max_abs_bf16x8(m2, w[j]);
+      m = bf16x2_max_to_float(m2);
+    } else {
+#pragma unroll
+      for (int j = 0; j < kRegVecs; ++j) m = max16<T>(w[j], m);
+    }
+    m = block_max(m, red);
+    sc = grid_scale<kFnuz>(m, g0, hdr, false);
   }
-  m = block_max(m, red);
-  const float sc = grid_scale<kFnuz>(m, g0, hdr, false);
   if (blockIdx.x == 0 && threadIdx.x == 0 && scale_out) *scale_out = sc;
   const float r = __frcp_rn(sc);
   const bool fast_ok = recip_is_normal(sc, r);
@@ -597,10 +605,14 @@ __global__ void __maxnreg__(48) quantize_regs_kernel(
 }
 
 // Shared-memory path: CTA b holds the contiguous elements [b per_cta, +per_cta).
+// With a static scale there is no amax and no barrier (and no header): each
+// chunk is encoded as soon as its copy lands, so the slice streams through
+// shared memory.
 template <typename T, bool kFnuz>
 __global__ void __launch_bounds__(kResThreads, 1) quantize_resident_kernel(
     const T* __restrict__ x, int64_t n, int64_t per_cta, uint8_t* __restrict__ q,
-    float* __restrict__ scale_out, unsigned* __restrict__ hdr) {
+    float* __restrict__ scale_out, unsigned* __restrict__ hdr,
+    const float* __restrict__ static_scale) {
   constexpr int VEC = 16 / sizeof(T);
   extern __shared__ __align__(128) uint8_t res[];
   __shared__ uint64_t bars[kResMaxChunks];
@@ -619,7 +631,7 @@ __global__ void __launch_bounds__(kResThreads, 1) quantize_resident_kernel(
   dev::grid_dependency_wait();  // x may come from the previous grid
   unsigned g0 = 0;
   if (tid == 0) {
-    g0 = ld_relaxed_gpu(hdr + 2);  // the previous grid is complete
+    if (!static_scale) g0 = ld_relaxed_gpu(hdr + 2);  // the previous grid is complete
     const uint64_t pol = dev::policy_evict_first();
     const uint8_t* src = reinterpret_cast<const uint8_t*>(x + e0);
     for (int i = 0; i < nchunks; ++i) {
@@ -628,6 +640,31 @@ __global__ void __launch_bounds__(kResThreads, 1) quantize_resident_kernel(
       dev::bulk_load(dev::smem_u32(res + i * kResChunk), src + i * kResChunk, sz, bar0 + 8 * i,
                      pol);
     }
+  }
+  if (static_scale) {
+    const float sc = __ldg(static_scale);
+    if (blockIdx.x == 0 && tid == 0 && scale_out) *scale_out = sc;
+    const float r = __frcp_rn(sc);
+    const bool fast_ok = recip_is_normal(sc, r);
+    // each chunk as soon as its copy lands (bounded; a copy that never
+    // lands leaves NaN codes for its chunk, so the result is visibly invalid)
+    for (int i = 0; i < nchunks; ++i) {
+      const bool landed = dev::mbar_wait(bar0 + 8 * i, 0, nullptr, nullptr, 0);
+      const uint32_t v0 = static_cast<uint32_t>(i) * (kResChunk / 16);
+      const uint32_t v1 = min(bytes / 16, v0 + kResChunk / 16);
+      if (landed) {
+        for (uint32_t v = v0 + tid; v < v1; v += kResThreads)
+          encode16<T, kFnuz>(*reinterpret_cast<const uint4*>(res + v * 16), sc, r, fast_ok,
+                             q + e0 + static_cast<int64_t>(v) * VEC);
+      } else {
+        for (uint32_t b = v0 * VEC + tid; b < v1 * VEC; b += kResThreads)
+          q[e0 + b] = kFnuz ? 0x80u : 0x7Fu;
+      }
+    }
+    // (the next grid's CTAs cannot share the SM with this one's shared
+    // memory anyway: let it go only now, so that it does not compete)
+    dev::grid_launch_dependents();
+    return;
   }
   // max |x| of the slice, chunk by chunk as the copies land (NaN is ignored
   // by fmaxf)
@@ -714,6 +751,43 @@ int tensor_grid(int64_t total_vecs, int per_sm, int limit) {
   return static_cast<int>(g < 1 ? 1 : g);
 }
 
+// Blocks of a kQThreads-thread kernel (no dynamic shared memory) resident per
+// SM, queried once per device.  The two-kernel path sizes its grids to one
+// wave: a dependent grid's blocks, launched early and waiting, then never hold
+// the SM slots that later blocks of this grid would need.
+template <typename Kern>
+int blocks_per_sm(Kern kern, int* cache) {
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();
+    return 4;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kQThreads, 0) != cudaSuccess ||
+        n < 1) {
+      cudaGetLastError();
+      n = 4;
+    }
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+template <typename T, int VEC>
+int amax_blocks_per_sm() {
+  static int cache[64] = {0};
+  return blocks_per_sm(amax_tensor_kernel<T, VEC>, cache);
+}
+
+template <typename T, int VEC, bool kFnuz>
+int encode_blocks_per_sm() {
+  static int cache[64] = {0};
+  return blocks_per_sm(encode_tensor_kernel<T, VEC, kFnuz>, cache);
+}
+
 // Sets the resident kernel's dynamic shared memory limit once per device.
 template <typename T, bool kFnuz>
 bool resident_ready() {
@@ -745,7 +819,9 @@ frt_status quantize_typed(const T* x, int64_t rows, int64_t cols, int64_t ldx, f
     const int64_t n = rows * cols;
     const int sms = sm_count() > 0 ? sm_count() : 148;
     const int64_t n_vec16 = n * static_cast<int64_t>(sizeof(T)) / 16;
-    if (!static_scale && vec && ldx == cols && aligned(ws_all, 16) &&
+    // (a static scale needs no workspace: no amax, no barrier)
+    const bool ws_ok = static_scale || aligned(ws_all, 16);
+    if (vec && ldx == cols && ws_ok &&
         n_vec16 <= static_cast<int64_t>(sms) * kRegThreads * kRegVecs) {
       // one grid, the tensor in registers: at most one CTA per SM
       const int grid = static_cast<int>(
@@ -760,14 +836,14 @@ frt_status quantize_typed(const T* x, int64_t rows, int64_t cols, int64_t ldx, f
       cfg.attrs = attr;
       cfg.numAttrs = 1;
       if (cudaLaunchKernelEx(&cfg, quantize_regs_kernel<T, kFnuz>, x, n_vec16, q, scale,
-                             hdr) != cudaSuccess) {
+                             static_scale ? nullptr : hdr, static_scale) != cudaSuccess) {
         cudaGetLastError();
         return FRT_ERR_CUDA;
       }
       note_launches(1);
       return launch_status();
     }
-    if (!static_scale && vec && ldx == cols && aligned(ws_all, 16) &&
+    if (vec && ldx == cols && ws_ok &&
         n * static_cast<int64_t>(sizeof(T)) <= static_cast<int64_t>(sms) * kResSmem &&
         resident_ready<T, kFnuz>()) {
       // one grid, the tensor resident in shared memory: slices of a multiple
@@ -789,7 +865,7 @@ frt_status quantize_typed(const T* x, int64_t rows, int64_t cols, int64_t ldx, f
       cfg.attrs = attr;
       cfg.numAttrs = 1;
       if (cudaLaunchKernelEx(&cfg, quantize_resident_kernel<T, kFnuz>, x, n, per, q, scale,
-                             hdr) != cudaSuccess) {
+                             static_scale ? nullptr : hdr, static_scale) != cudaSuccess) {
         cudaGetLastError();
         return FRT_ERR_CUDA;
       }
@@ -797,8 +873,12 @@ frt_status quantize_typed(const T* x, int64_t rows, int64_t cols, int64_t ldx, f
       return launch_status();
     }
     const int64_t total = rows * (vec ? cols / 8 : cols);
-    const int grid = tensor_grid(total, 6, kMaxPartials);  // amax: one partial per block
-    const int egrid = tensor_grid(total, 8, 1 << 20);
+    // one wave each; amax: one partial per block
+    const int grid = tensor_grid(
+        total, vec ? amax_blocks_per_sm<T, 8>() : amax_blocks_per_sm<T, 1>(), kMaxPartials);
+    const int egrid = tensor_grid(
+        total, vec ? encode_blocks_per_sm<T, 8, kFnuz>() : encode_blocks_per_sm<T, 1, kFnuz>(),
+        1 << 20);
     // programmatic launches: each kernel's blocks may be scheduled while the
     // previous grid drains, and wait for it before reading its output
     cudaLaunchConfig_t cfg = {};

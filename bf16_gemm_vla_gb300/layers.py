@@ -61,6 +61,10 @@ class Linear:
     FP8:  q, s = quantize(x) per tensor (OCP); out = gemm_fp8(q, s, W).
     BF16: out = gemm_bf16(x, W).
     ``act_cols`` output columns get the tanh-GELU.
+
+    FP8 activation scales are dynamic (amax of every input) until
+    ``calibrate`` freezes one: then each call only encodes with it (one
+    pass over x instead of amax + encode).
     """
 
     def __init__(self, weight: PackedWeight, M, act_cols=0, out=None, device=None):
@@ -75,15 +79,41 @@ class Linear:
             self.a_scale = torch.empty((1,), dtype=torch.float32, device=dev)
             nb = frt.frt_quantize_workspace_bytes(M, weight.K, frt.PER_TENSOR)
             self.ws = torch.zeros((max(nb, 4) // 4,), dtype=torch.float32, device=dev)
+            self.static = False
+            self.s_out = torch.empty((1,), dtype=torch.float32, device=dev)  # static path's copy
         # the GEMM's own (zero-filled) workspace, or False if it needs none
         gws = frt.gemm_workspace(M, weight.N, weight.K, weight.kind, dev)
         self.gws = False if gws is None else gws
 
+    def calibrate(self, xs, stream=None):
+        """Freezes the activation scale at the largest dynamic scale over the
+        calibration inputs ``xs`` (each [M x K] bf16): s = max_i amax_i / 448,
+        which is the dynamic scale of all of them together since the rounded
+        division is monotone.  Later calls encode with it; inputs beyond the
+        calibrated range saturate to +-448.  Load-time: synchronises."""
+        if self.w.kind != "e4m3":
+            raise ValueError("calibrate applies to FP8 layers")
+        best = None
+        for x in xs:
+            frt.frt_quantize_e4m3(x, frt.PER_TENSOR, frt.OCP, q=self.q, scale=self.a_scale,
+                                  workspace=self.ws, stream=stream)
+            torch.cuda.synchronize(self.a_scale.device)
+            s = float(self.a_scale.cpu()[0])
+            best = s if best is None or s > best else best
+        self.a_scale.fill_(best)
+        torch.cuda.synchronize(self.a_scale.device)
+        self.static = True
+        return best
+
     def __call__(self, x, stream=None):
         w = self.w
         if w.kind == "e4m3":
-            frt.frt_quantize_e4m3(x, frt.PER_TENSOR, frt.OCP, q=self.q, scale=self.a_scale,
-                                  workspace=self.ws, stream=stream)
+            if self.static:
+                frt.frt_quantize_e4m3(x, frt.PER_TENSOR, frt.OCP, static_scale=self.a_scale,
+                                      q=self.q, scale=self.s_out, stream=stream)
+            else:
+                frt.frt_quantize_e4m3(x, frt.PER_TENSOR, frt.OCP, q=self.q, scale=self.a_scale,
+                                      workspace=self.ws, stream=stream)
             return frt.frt_gemm_fp8(self.q, self.a_scale, w.packed, w.w_scale, w.N, bias=w.bias,
                                     act_cols=self.act_cols, out=self.out, stream=stream,
                                     workspace=self.gws)

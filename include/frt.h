@@ -104,7 +104,9 @@ const char* frt_status_string(frt_status status);
  * out_fmt   : FRT_E4M3_OCP or FRT_E4M3_FNUZ.
  * static_scale: NULL -> compute amax and s as above.  Non-NULL -> device
  *           pointer to the scale(s) to use (1 float, or `cols` floats per
- *           column); amax is skipped and the workspace is not used.
+ *           column); amax is skipped and the workspace is not used (per
+ *           tensor, a dense aligned x is encoded in one pass as its parts
+ *           arrive on chip: no barrier between the CTAs).
  * q         : [rows x cols] bytes, contiguous (row stride cols).
  * scale     : device, receives s (1 float, or `cols` floats); may be NULL.
  * workspace : device memory of frt_quantize_workspace_bytes() bytes, 4-byte
