@@ -23,7 +23,7 @@ FRT_F32, FRT_BF16, FRT_E4M3_OCP, FRT_E4M3_FNUZ = 0, 1, 2, 3
 # frt_scale_mode
 FRT_SCALE_PER_TENSOR, FRT_SCALE_PER_COL = 0, 1
 # frt_act
-FRT_ACT_NONE, FRT_ACT_GELU_TANH = 0, 1
+FRT_ACT_NONE, FRT_ACT_GELU_TANH, FRT_ACT_GEGLU = 0, 1, 2
 
 _c_i64 = ctypes.c_int64
 _c_sz = ctypes.c_size_t

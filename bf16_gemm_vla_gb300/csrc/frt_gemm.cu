@@ -78,6 +78,11 @@ struct GemmArgs {
   const float* bias;     // N floats or null (= 0)
   int M, N;
   int act_cols;
+  // merged gate/up GEMM with the GeGLU fused (pairs, 256-wide tiles): the
+  // tile's CTAs hold gate channel group tn and up group f_groups + tn, and
+  // the output is gelu(gate) * up, 128 columns per tile
+  int geglu;
+  int f_groups;  // F / 128, F = N / 2
   int kb_total;  // 128-byte K blocks of the packed weight
   int nb_total;  // 128-channel groups of the packed weight
   int kb_per_split;
@@ -368,7 +373,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // 256-channel tiles: one 128-channel group per CTA; 128-channel
           // tiles: one half group per CTA.  Both CTAs' copies complete on
           // the leader's barrier.
-          nbf = kBN == 256 ? 2 * tn + px : tn;
+          nbf = kBN == 256 ? (p.geglu ? (px ? p.f_groups + tn : tn) : 2 * tn + px) : tn;
           groups = 1;
           return 2u * stage_bytes;  // whole boxes (zero fill counts)
         }
@@ -587,7 +592,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       float wsc[kColsPerThread], wbi[kColsPerThread];
 #pragma unroll
       for (int j = 0; j < kColsPerThread; ++j) {
-        const int n = kSwap ? tn * kTile + row : tn * kBN + et + 128 * j;
+        const int n = kSwap ? tn * kTile + row
+                            : (p.geglu ? (j ? p.f_groups : 0) * kTile + tn * kTile + et
+                                       : tn * kBN + et + 128 * j);
         wsc[j] = n < p.N ? (p.w_scale ? __ldg(p.w_scale + n) : 1.0f) : 0.0f;
         wbi[j] = (n < p.N && p.bias) ? __ldg(p.bias + n) : 0.0f;
       }
@@ -665,7 +672,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
 
       if (!split) {
-        if constexpr (kBN >= 64) {
+        if (kPair && kBN == 256 && p.geglu) {
+          if constexpr (kPair && kBN == 256) {
+          // ------------- fused GeGLU: columns [0, 128) hold the gate, [128,
+          // 256) the up channels of the same 128 outputs
+#pragma unroll 1
+          for (int c = 0; c < 128; c += 32) {
+            float g[32], u[32];
+            dev::tmem_ld32(tacc + c, g);
+            dev::tmem_ld32(tacc + 128 + c, u);
+            if (c + 32 == 128 && it + 1 < my_tiles) release_acc(b);
+            const float4* gs4 = reinterpret_cast<const float4*>(cs_s + c);
+            const float4* gb4 = reinterpret_cast<const float4*>(cb_s + c);
+            const float4* us4 = reinterpret_cast<const float4*>(cs_s + 128 + c);
+            const float4* ub4 = reinterpret_cast<const float4*>(cb_s + 128 + c);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              const float4 gs = gs4[q], gb = gb4[q], us = us4[q], ub = ub4[q];
+              g[4 * q + 0] = gelu_tanh(lin(g[4 * q + 0], gs.x, gb.x)) * lin(u[4 * q + 0], us.x, ub.x);
+              g[4 * q + 1] = gelu_tanh(lin(g[4 * q + 1], gs.y, gb.y)) * lin(u[4 * q + 1], us.y, ub.y);
+              g[4 * q + 2] = gelu_tanh(lin(g[4 * q + 2], gs.z, gb.z)) * lin(u[4 * q + 2], us.z, ub.z);
+              g[4 * q + 3] = gelu_tanh(lin(g[4 * q + 3], gs.w, gb.w)) * lin(u[4 * q + 3], us.w, ub.w);
+            }
+            warp_store<false, 32>(g, wbuf + wb * kWarpOutBytes, wbuf_s + wb * kWarpOutBytes,
+                                  &tmap_out, tn * kTile + c, row0 + ew * 32, lane);
+            wb ^= 1;
+          }
+          }
+        } else if constexpr (kBN >= 64) {
 #pragma unroll 1
           for (int c = 0; c < kBN; c += 64) {
             float v[64];
@@ -1001,6 +1035,7 @@ struct Plan {
   int kbs;  // k-blocks per stage
   bool recv_in_stages;
   bool split_global;  // split-K through the workspace (CTA pairs)
+  bool geglu;         // merged gate/up with the GeGLU fused: 256-wide pair tiles, no split
   size_t ws_bytes;    // workspace the plan uses (split_global), else 0
   size_t ws_flag_bytes;
   int outbuf_off, recv_off, tail_off;
@@ -1151,9 +1186,11 @@ void global_split_bytes(Plan& pl) {
                                        static_cast<size_t>(kTile * pl.chunk_cols * 4);
 }
 
-Plan make_plan(int64_t M, int64_t N, int64_t K, int esize, bool fp8, size_t ws_avail) {
+Plan make_plan(int64_t M, int64_t N, int64_t K, int esize, bool fp8, size_t ws_avail,
+               bool geglu = false) {
   Plan pl;
   pl.split_global = false;
+  pl.geglu = geglu;
   pl.ws_bytes = 0;
   pl.ws_flag_bytes = 0;
   const int kb = static_cast<int>(ceil_div(K * esize, kKBytes));
@@ -1177,7 +1214,7 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int esize, bool fp8, size_t ws_a
     pl.tiles_m = static_cast<int>(ceil_div(M, 2 * kTile));
     const int64_t wide = 2 * pl.tiles_m * ceil_div(N, 256);  // CTAs
     const int64_t narrow = 2 * pl.tiles_m * ceil_div(N, 128);
-    pl.bn = (2 * wide <= sms && narrow <= sms && kb <= 32) ? 128 : 256;
+    pl.bn = (!geglu && 2 * wide <= sms && narrow <= sms && kb <= 32) ? 128 : 256;
     pl.tiles_n = static_cast<int>(ceil_div(N, pl.bn));
     pl.chunk_cols = 32;
   }
@@ -1199,7 +1236,7 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int esize, bool fp8, size_t ws_a
   };
 
   int s_max = 1, g_max = 1;
-  if (pl.num_tiles * ctas_per_tile < sms) {
+  if (pl.num_tiles * ctas_per_tile < sms && !geglu) {  // (a GeGLU tile is finished whole)
     s_max = sms / (pl.num_tiles * ctas_per_tile);
     const int nchunks = pl.bn / pl.chunk_cols;
     if (s_max > nchunks) s_max = nchunks;
@@ -1318,10 +1355,14 @@ frt_status gemm_common(bool fp8, const void* a, int64_t lda, const float* a_scal
   const int esize = fp8 ? 1 : 2;
   if (!a || !w_packed || !out) return FRT_ERR_INVALID_ARG;
   if (fp8 && (!a_scale || !w_scale)) return FRT_ERR_INVALID_ARG;
-  if (act != FRT_ACT_NONE && act != FRT_ACT_GELU_TANH) return FRT_ERR_INVALID_ARG;
+  if (act != FRT_ACT_NONE && act != FRT_ACT_GELU_TANH && act != FRT_ACT_GEGLU)
+    return FRT_ERR_INVALID_ARG;
   if (M < 1 || N < 1 || K < 1) return FRT_ERR_INVALID_ARG;
   if (act == FRT_ACT_GELU_TANH && (act_cols < 0 || act_cols > N)) return FRT_ERR_INVALID_ARG;
-  if (lda < K || ldo < N) return FRT_ERR_INVALID_ARG;
+  const bool geglu = act == FRT_ACT_GEGLU;
+  const int64_t n_out = geglu ? N / 2 : N;  // GeGLU: gelu(gate) * up, N / 2 columns
+  if (lda < K || ldo < n_out) return FRT_ERR_INVALID_ARG;
+  if (geglu && (M <= 128 || N % 256 != 0)) return FRT_ERR_UNSUPPORTED_SHAPE;
   if (ldo > (1LL << 31) - 1) return FRT_ERR_UNSUPPORTED_SHAPE;
   if (N % 16 != 0 || K % (fp8 ? 32 : 16) != 0) return FRT_ERR_UNSUPPORTED_SHAPE;
   if (M > (1LL << 31) - 1 || N > (1LL << 31) - 1 || K > (1LL << 31) - 1)
@@ -1341,7 +1382,7 @@ frt_status gemm_common(bool fp8, const void* a, int64_t lda, const float* a_scal
   if (!encode) return FRT_ERR_CUDA;
   // a workspace that is missing or misaligned is not used
   const size_t ws_avail = (workspace && aligned(workspace, 256)) ? workspace_bytes : 0;
-  const Plan pl = make_plan(M, N, K, esize, fp8, ws_avail);
+  const Plan pl = make_plan(M, N, K, esize, fp8, ws_avail, geglu);
 
   CUtensorMap ta, tw, to;
   if (pl.kbs > 1) {
@@ -1394,7 +1435,7 @@ frt_status gemm_common(bool fp8, const void* a, int64_t lda, const float* a_scal
   {
     // output boxes, one per epilogue warp and chunk: {32 channels, 32 rows}
     // (small M split-K: {32 channels, 8 rows}), 64-byte swizzle
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(M)};
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(n_out), static_cast<cuuint64_t>(M)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ldo * 2)};
     const cuuint32_t box[2] = {32u, (pl.swap && pl.splits > 1) ? 8u : 32u};
     const cuuint32_t estr[2] = {1, 1};
@@ -1412,6 +1453,8 @@ frt_status gemm_common(bool fp8, const void* a, int64_t lda, const float* a_scal
   ga.M = static_cast<int>(M);
   ga.N = static_cast<int>(N);
   ga.act_cols = act == FRT_ACT_GELU_TANH ? static_cast<int>(act_cols) : 0;
+  ga.geglu = geglu ? 1 : 0;
+  ga.f_groups = geglu ? static_cast<int>(N / 256) : 0;
   ga.kb_total = static_cast<int>(kb_total);
   ga.nb_total = static_cast<int>(nb_total);
   ga.kb_per_split = pl.kb_per_split;

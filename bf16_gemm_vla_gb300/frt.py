@@ -240,15 +240,23 @@ def _gemm_out(M, N, out, device):
     return out, ldo
 
 
+def _act(act_cols, geglu):
+    if geglu:
+        return _lib.FRT_ACT_GEGLU, 0
+    return (_lib.FRT_ACT_GELU_TANH if act_cols else _lib.FRT_ACT_NONE), act_cols
+
+
 def frt_gemm_fp8(a_q, a_scale, w_packed, w_scale, N, bias=None, act_cols=0, out=None,
-                 stream=None, workspace=None):
+                 stream=None, workspace=None, geglu=False):
     """out = bf16(act(a_scale * w_scale[n] * (A_q . W) + bias[n])), GELU on
     the first act_cols columns.  a_q: [M x K] OCP E4M3 bytes.  workspace: a
     zero-filled uint8 tensor of frt_gemm_workspace_bytes() bytes, False for
-    none, or None for the shared per-device one."""
+    none, or None for the shared per-device one.  geglu: W is a merged
+    gate/up weight (gate channels first) and out = gelu(gate) * up, N / 2
+    columns."""
     M, K, lda = _rows_view(a_q, "a_q")
-    out, ldo = _gemm_out(M, N, out, a_q.device)
-    act = _lib.FRT_ACT_GELU_TANH if act_cols else _lib.FRT_ACT_NONE
+    out, ldo = _gemm_out(M, N // 2 if geglu else N, out, a_q.device)
+    act, act_cols = _act(act_cols, geglu)
     wp, wb = _gemm_ws(workspace, M, N, K, "e4m3", a_q.device)
     _check("frt_gemm_fp8",
            lib().frt_gemm_fp8(a_q.data_ptr(), lda, _ptr(a_scale), w_packed.data_ptr(),
@@ -259,12 +267,12 @@ def frt_gemm_fp8(a_q, a_scale, w_packed, w_scale, N, bias=None, act_cols=0, out=
 
 
 def frt_gemm_bf16(a, w_packed, N, w_scale=None, bias=None, act_cols=0, out=None, stream=None,
-                  workspace=None):
+                  workspace=None, geglu=False):
     """out = bf16(act(w_scale[n] * (A . W) + bias[n])).  a: [M x K] bf16.
-    workspace as for frt_gemm_fp8."""
+    workspace and geglu as for frt_gemm_fp8."""
     M, K, lda = _rows_view(a, "a")
-    out, ldo = _gemm_out(M, N, out, a.device)
-    act = _lib.FRT_ACT_GELU_TANH if act_cols else _lib.FRT_ACT_NONE
+    out, ldo = _gemm_out(M, N // 2 if geglu else N, out, a.device)
+    act, act_cols = _act(act_cols, geglu)
     wp, wb = _gemm_ws(workspace, M, N, K, "bf16", a.device)
     _check("frt_gemm_bf16",
            lib().frt_gemm_bf16(a.data_ptr(), lda, w_packed.data_ptr(), _ptr(w_scale), _ptr(bias),

@@ -72,7 +72,8 @@ typedef enum {
 
 typedef enum {
   FRT_ACT_NONE = 0,
-  FRT_ACT_GELU_TANH = 1 /* 0.5 v (1 + tanh(sqrt(2/pi) (v + 0.044715 v^3))) */
+  FRT_ACT_GELU_TANH = 1, /* 0.5 v (1 + tanh(sqrt(2/pi) (v + 0.044715 v^3))) */
+  FRT_ACT_GEGLU = 2      /* merged gate/up: out = gelu_tanh(v_gate) * v_up, N / 2 columns */
 } frt_act;
 
 /* Version of this ABI (incremented on any signature change). */
@@ -219,6 +220,13 @@ frt_status frt_pack_weights(const void* w, frt_dtype w_dtype, int64_t K, int64_t
  *   v         = acc * (a_scale * w_scale[n]) + bias[n]
  *   v         = gelu_tanh(v)   if act == FRT_ACT_GELU_TANH and n < act_cols
  *   out[m, n] = bf16(v)        (round to nearest even)
+ *
+ * act == FRT_ACT_GEGLU fuses the GeGLU of a merged gate/up layer ("Merging
+ * gate and up"): w is [K x N] with the gate's F = N / 2 channels first and
+ * the up channels after them (w_scale and bias likewise, N floats), and
+ *   out[m, j] = bf16(gelu_tanh(v[m, j]) * v[m, F + j]),  0 <= j < F,
+ * so out is [M x F] (ldo >= F); act_cols is ignored.  Requires M > 128 and
+ * N % 256 == 0 (else FRT_ERR_UNSUPPORTED_SHAPE).
  *
  * a_q / a   : [M x K] row-major, row stride lda; E4M3 OCP bytes (FP8) or
  *             bf16 (BF16); 16-byte aligned, lda * esize a multiple of 16.

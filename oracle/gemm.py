@@ -18,7 +18,9 @@ GELU.  The result stays fp64; the final bf16 store is the kernel's rounding,
 covered by the comparison tolerance.
 
 The product sum uses numpy's fp64 matmul (BLAS dgemm) as a library primitive;
-``gemm_naive`` is the plain triple loop for tiny shapes.
+``gemm_naive`` is the plain triple loop for tiny shapes.  ``geglu`` is the
+fused GeGLU of a merged gate/up layer, applied to the layer's output without
+activation.
 """
 import math
 
@@ -79,6 +81,38 @@ def gemm_fp8(qa, a_fmt, a_scale, qw, w_fmt, w_scale, bias=None, act_cols=0):
 def gemm_bf16(a_f32, w_f32, w_scale=None, bias=None, act_cols=0):
     """BF16 layer on bf16 values given as fp32 arrays (exact)."""
     return gemm_values(a_f32, w_f32, None, w_scale, bias, act_cols)
+
+
+def gelu_tanh_prime(v):
+    """Derivative of the tanh-approximate GELU, in closed form (fp64):
+    0.5 (1 + t) + 0.5 v (1 - t^2) sqrt(2/pi) (1 + 3 * 0.044715 v^2) with
+    t = tanh(sqrt(2/pi) (v + 0.044715 v^3))."""
+    v = np.asarray(v, dtype=np.float64)
+    t = np.tanh(SQRT_2_OVER_PI * (v + 0.044715 * v * v * v))
+    return 0.5 * (1.0 + t) + 0.5 * v * (1.0 - t * t) * SQRT_2_OVER_PI * (
+        1.0 + 3.0 * 0.044715 * v * v)
+
+
+def geglu(y, sumabs):
+    """GeGLU of a merged gate/up layer ("Real-time VLA inference on AMD
+    hardware", section "Merging gate and up": one GEMM over [W_gate, W_up],
+    the gate's channels first): with y [M x N] the layer's output before any
+    activation (fp64) and F = N / 2,
+
+        h[m, j] = gelu_tanh(y[m, j]) * y[m, F + j],   0 <= j < F.
+
+    Returns (h [M x F], prop [M x F]): prop carries the magnitudes the
+    layer's sums are measured against through the product to first order,
+    |gelu_tanh'(g)| |u| sumabs_gate + |gelu_tanh(g)| sumabs_up, the
+    magnitude h's tolerance is measured against.
+    """
+    y = np.asarray(y, dtype=np.float64)
+    F = y.shape[1] // 2
+    g, u = y[:, :F], y[:, F:]
+    h = gelu_tanh(g) * u
+    prop = (np.abs(gelu_tanh_prime(g)) * np.abs(u) * sumabs[:, :F] +
+            np.abs(gelu_tanh(g)) * sumabs[:, F:])
+    return h, prop
 
 
 def gemm_naive(a, w):

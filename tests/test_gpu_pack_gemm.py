@@ -331,3 +331,55 @@ def test_plan_shapes_fp8_and_bf16(M, K, N):
     lay = rand_layer(M, K, N, seed=M + K + N)
     fp8_layer(lay)
     bf16_layer(lay)
+
+
+# ---------------------------------------------------------------- fused GeGLU (merged gate/up)
+
+def geglu_oracle(lay, qa_o, sa_o, qw_o, sw_o, kind):
+    if kind == "e4m3":
+        y, sumabs = gemm.gemm_fp8(qa_o, e4m3.OCP, sa_o, qw_o, e4m3.OCP, sw_o, lay["bias"], 0)
+    else:
+        y, sumabs = gemm.gemm_bf16(synth.bf16_bits_as_f32(lay["a_bf16"]),
+                                   obf16.round_to_bf16(lay["w_f32"]), None, lay["bias"], 0)
+    return gemm.geglu(y, sumabs)
+
+
+@pytest.mark.parametrize("M,K,F", [(300, 1024, 512), (257, 256, 128), (520, 1152, 1280),
+                                   (768, 2048, 16384)])
+@pytest.mark.parametrize("kind", ["e4m3", "bf16"])
+def test_geglu_fused_epilogue(M, K, F, kind):
+    # one GEMM over [W_gate, W_up] (2F channels, gate first) whose epilogue
+    # writes gelu(gate) * up: F output columns
+    lay = rand_layer(M, K, 2 * F, seed=M + K + F)
+    a_dev = bf16_dev(lay["a_bf16"])
+    b_dev = torch.from_numpy(lay["bias"]).cuda()
+    w_dev = torch.from_numpy(lay["w_f32"]).cuda()
+    qa_o = sa_o = qw_o = sw_o = None
+    if kind == "e4m3":
+        qa, sa = frt.frt_quantize_e4m3(a_dev, frt.PER_TENSOR, frt.OCP)
+        pw = layers.prepare_fp8(w_dev, b_dev)
+        out = frt.frt_gemm_fp8(qa, sa, pw.packed, pw.w_scale, 2 * F, bias=b_dev, geglu=True)
+        qa_o, sa_o = quantize.quantize_e4m3(synth.bf16_bits_as_f32(lay["a_bf16"]),
+                                            quantize.PER_TENSOR, e4m3.OCP)
+        qw_o, sw_o = quantize.quantize_e4m3(lay["w_f32"], quantize.PER_COL, e4m3.OCP)
+    else:
+        wp = frt.frt_pack_weights(w_dev, "bf16")
+        torch.cuda.synchronize()
+        out = frt.frt_gemm_bf16(a_dev, wp, 2 * F, bias=b_dev, geglu=True)
+    frt.check_device_status()
+    assert tuple(out.shape) == (M, F)
+    h, prop = geglu_oracle(lay, qa_o, sa_o, qw_o, sw_o, kind)
+    assert_gemm_close(out, h, prop, "geglu %s M=%d K=%d F=%d" % (kind, M, K, F))
+
+
+def test_geglu_rejects_unsupported_shapes():
+    a = torch.zeros((64, 256), dtype=torch.bfloat16, device="cuda")
+    wp = frt.frt_pack_weights(torch.zeros((256, 512), device="cuda"), "bf16")
+    torch.cuda.synchronize()
+    with pytest.raises(frt.FrtError):
+        frt.frt_gemm_bf16(a, wp, 512, geglu=True)  # M <= 128
+    a = torch.zeros((300, 256), dtype=torch.bfloat16, device="cuda")
+    wp = frt.frt_pack_weights(torch.zeros((256, 384), device="cuda"), "bf16")
+    torch.cuda.synchronize()
+    with pytest.raises(frt.FrtError):
+        frt.frt_gemm_bf16(a, wp, 384, geglu=True)  # N % 256 != 0

@@ -89,3 +89,30 @@ def test_tiny_fp8_layer_close_to_unquantized():
     ref, _ = gemm.gemm_values(a, t["w_f32"], None, None, t["bias"], 256)
     err = np.abs(y - ref)
     assert np.sqrt(np.mean(err ** 2)) / np.sqrt(np.mean(ref ** 2)) < 0.08
+
+
+def test_gelu_tanh_prime_against_central_differences():
+    # the closed form against (f(v + h) - f(v - h)) / 2h in fp64, and its
+    # limits: 0.5 at 0, 1 far right, 0 far left
+    v = np.array([-6.0, -2.5, -1.0, -0.3, 0.0, 0.4, 1.0, 1.7, 3.0, 6.0])
+    h = 1e-5
+    fd = (gemm.gelu_tanh(v + h) - gemm.gelu_tanh(v - h)) / (2 * h)
+    np.testing.assert_allclose(gemm.gelu_tanh_prime(v), fd, rtol=1e-8, atol=1e-9)
+    assert gemm.gelu_tanh_prime(0.0) == 0.5
+    assert abs(gemm.gelu_tanh_prime(20.0) - 1.0) < 1e-12
+    assert abs(gemm.gelu_tanh_prime(-20.0)) < 1e-12
+
+
+def test_geglu_gate_first_and_propagated_magnitude():
+    # y = [g0 g1 | u0 u1]: h = [gelu(g0) u0, gelu(g1) u1]; a swapped split
+    # (up first) or a missing product would give other values
+    y = np.array([[1.0, -2.0, 3.0, 5.0], [0.0, 10.0, 7.0, -0.5]])
+    s = np.array([[1.0, 2.0, 3.0, 4.0], [5.0, 6.0, 7.0, 8.0]])
+    hh, prop = gemm.geglu(y, s)
+    g = lambda v: 0.5 * v * (1.0 + math.tanh(math.sqrt(2.0 / math.pi) * (v + 0.044715 * v ** 3)))  # noqa: E731
+    np.testing.assert_allclose(hh, [[g(1.0) * 3.0, g(-2.0) * 5.0], [0.0, g(10.0) * -0.5]],
+                               rtol=1e-15, atol=0)
+    # gelu(0) = 0: the up magnitude does not count, the gate's does at 0.5 |u|
+    assert prop[1, 0] == 0.5 * 7.0 * 5.0
+    # far right, gelu(g) = g and gelu'(g) = 1
+    assert abs(prop[1, 1] - (0.5 * 6.0 + 10.0 * 8.0)) < 1e-9
