@@ -521,9 +521,10 @@ def run_headline(args, device, world, sampler, peaks, peak_kind):
 
 # ---------------------------------------------------------------- components
 
-def gemm_stream_rate(lay, kind, device, sampler, reps=3):
+def gemm_stream_rate(lay, kind, device, sampler, reps=3, geglu=False):
     """Per-launch device time of one layer's GEMM, over rotating weight copies
-    (total > 4x L2) captured back to back in one graph."""
+    (total > 4x L2) captured back to back in one graph.  geglu: the layer is a
+    merged gate/up and the GEMM writes gelu(gate) * up (N / 2 columns)."""
     from bf16_gemm_vla_gb300 import frt, layers
 
     w = torch.from_numpy(lay["w_f32"]).to(device)
@@ -539,15 +540,17 @@ def gemm_stream_rate(lay, kind, device, sampler, reps=3):
     if kind == "e4m3":
         frt.frt_quantize_e4m3(x, frt.PER_TENSOR, frt.OCP, q=lin.q, scale=lin.a_scale,
                               workspace=lin.ws)
+    out = lin.out[:, :pw.N // 2] if geglu else lin.out
+    act_cols = 0 if geglu else lay["act_cols"]
 
     def run_all():
         for p in packs:
             if kind == "e4m3":
                 frt.frt_gemm_fp8(lin.q, lin.a_scale, p, pw.w_scale, pw.N, bias=b,
-                                 act_cols=lay["act_cols"], out=lin.out, workspace=lin.gws)
+                                 act_cols=act_cols, out=out, workspace=lin.gws, geglu=geglu)
             else:
-                frt.frt_gemm_bf16(x, p, pw.N, bias=b, act_cols=lay["act_cols"], out=lin.out,
-                                  workspace=lin.gws)
+                frt.frt_gemm_bf16(x, p, pw.N, bias=b, act_cols=act_cols, out=out,
+                                  workspace=lin.gws, geglu=geglu)
 
     g = capture(run_all)
     g.replay()
@@ -583,6 +586,19 @@ def run_components(args, device, sampler, peaks):
     out["encoder_m768_bf16"] = {"layers": rows, "tflops": tf / tt / 1e12,
                                 "frac_of_bf16_peak": tf / tt / 1e12 / peaks["bf16_tflops_sustained"]}
     del enc
+    # the merged encoder gate/up (2048 -> 2 x 16384, the stack's FFN) at M=768:
+    # one GEMM writing both halves (GELU on the gate half) against the same
+    # GEMM with the GeGLU fused (gelu(gate) * up, half the output)
+    gu = synth.layer(np.random.default_rng(7), M_ENC, 2048, 2 * 16384, act_cols=16384,
+                     outlier_frac=0.01)
+    fl = 2.0 * M_ENC * 2048 * 2 * 16384
+    both = {"unfused": gemm_stream_rate(gu, "e4m3", device, sampler, reps=2),
+            "fused_geglu": gemm_stream_rate(gu, "e4m3", device, sampler, reps=2, geglu=True)}
+    for v in both.values():
+        v["frac_of_fp8_peak"] = fl / (v["us"] * 1e-6) / 1e12 / (
+            peaks["bf16_tflops_sustained"] * FP8_OVER_BF16)
+    out["encoder_gate_up_fp8_m768"] = both
+    del gu
     # the encoder FP8 step with each layer's activation scale calibrated once
     # (on that layer's input) and frozen: the quantize is one encode pass
     set0 = EncoderFP8Set(synth.encoder(seed=0, M=M_ENC), device)

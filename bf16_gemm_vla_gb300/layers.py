@@ -67,12 +67,16 @@ class Linear:
     pass over x instead of amax + encode).
     """
 
-    def __init__(self, weight: PackedWeight, M, act_cols=0, out=None, device=None):
+    def __init__(self, weight: PackedWeight, M, act_cols=0, out=None, device=None, geglu=False):
         self.w = weight
         self.M = M
         self.act_cols = act_cols
+        # merged gate/up (gate channels first) with the GeGLU fused: the
+        # output is gelu(gate) * up, N / 2 columns
+        self.geglu = geglu
         dev = device if device is not None else weight.packed.device
-        self.out = out if out is not None else torch.empty((M, weight.N), dtype=torch.bfloat16,
+        n_out = weight.N // 2 if geglu else weight.N
+        self.out = out if out is not None else torch.empty((M, n_out), dtype=torch.bfloat16,
                                                             device=dev)
         if weight.kind == "e4m3":
             self.q = torch.empty((M, weight.K), dtype=torch.uint8, device=dev)
@@ -116,7 +120,7 @@ class Linear:
                                       workspace=self.ws, stream=stream)
             return frt.frt_gemm_fp8(self.q, self.a_scale, w.packed, w.w_scale, w.N, bias=w.bias,
                                     act_cols=self.act_cols, out=self.out, stream=stream,
-                                    workspace=self.gws)
+                                    workspace=self.gws, geglu=self.geglu)
         return frt.frt_gemm_bf16(x, w.packed, w.N, w_scale=w.w_scale, bias=w.bias,
                                  act_cols=self.act_cols, out=self.out, stream=stream,
-                                 workspace=self.gws)
+                                 workspace=self.gws, geglu=self.geglu)
