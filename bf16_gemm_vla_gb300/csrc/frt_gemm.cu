@@ -652,10 +652,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             v[4 * q + 2] = lin(v[4 * q + 2], sc.z, bi.z);
             v[4 * q + 3] = lin(v[4 * q + 3], sc.w, bi.w);
           }
-          if (n0 < p.act_cols) {  // uniform across the warp: the chunk's columns
+          // (uniform across the warp: the chunk's columns).  The GELUs are
+          // evaluated without a branch per element, so that the 32
+          // independent evaluations interleave; a chunk that straddles
+          // act_cols selects per element.
+          if (n0 + 32 <= p.act_cols) {
 #pragma unroll
-            for (int j = 0; j < 32; ++j)
-              if (n0 + j < p.act_cols) v[j] = gelu_tanh(v[j]);
+            for (int j = 0; j < 32; ++j) v[j] = gelu_tanh(v[j]);
+          } else if (n0 < p.act_cols) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const float gv = gelu_tanh(v[j]);
+              v[j] = n0 + j < p.act_cols ? gv : v[j];
+            }
           }
           warp_store<false, 32>(v, wbuf + wb * kWarpOutBytes, wbuf_s + wb * kWarpOutBytes,
                                 &tmap_out, n0, row0 + ew * 32, lane);
