@@ -78,9 +78,11 @@ struct GemmArgs {
   const float* bias;     // N floats or null (= 0)
   int M, N;
   int act_cols;
-  // merged gate/up GEMM with the GeGLU fused (pairs, 256-wide tiles): the
-  // tile's CTAs hold gate channel group tn and up group f_groups + tn, and
-  // the output is gelu(gate) * up, 128 columns per tile
+  // merged gate/up GEMM with the GeGLU fused: the output is gelu(gate) *
+  // up.  Pairs (256-wide tiles): the tile's CTAs hold gate channel group tn
+  // and up group f_groups + tn, 128 outputs per tile.  Small M: a tile's
+  // 128 weight rows are 64 gate channels (64 tn ..) and the 64 up channels
+  // of the same outputs, 64 outputs per tile.
   int geglu;
   int f_groups;  // F / 128, F = N / 2
   int kb_total;  // 128-byte K blocks of the packed weight
@@ -406,9 +408,30 @@ __global__ void __launch_bounds__(kThreads, 1)
           dev::tma_load_3d_pair(st + act_bytes, &tmap_w, 0, half * (kTile / 2),
                                 nbf * p.kb_total + kb, full_bar(s), pol_w);
         } else if constexpr (kSwap) {
-          const uint8_t* src = p.w_packed + (static_cast<size_t>(nbf) * p.kb_total + kb) * kWTile;
-          dev::bulk_load(st + act_bytes, src, static_cast<uint32_t>(groups * kWTile), full0 + 8 * s,
-                         pol_w);
+          if (p.geglu) {
+            // rows 0-63: gate channels 64 nbf .. of the packed group nbf / 2,
+            // rows 64-127: the up channels F + 64 nbf ..; a packed tile's rows
+            // are 128 bytes, so a half group of one k-tile is 8 KiB (the
+            // 128-byte swizzle repeats every 8 rows, so the halves keep it)
+            const size_t half = static_cast<size_t>(nbf & 1) * (kWTile / 2);
+            for (int q = 0; q < groups; ++q) {
+              const uint8_t* sg = p.w_packed +
+                                  (static_cast<size_t>(nbf >> 1) * p.kb_total + kb + q) * kWTile +
+                                  half;
+              const uint8_t* su =
+                  p.w_packed +
+                  (static_cast<size_t>(p.f_groups + (nbf >> 1)) * p.kb_total + kb + q) * kWTile +
+                  half;
+              const uint32_t dst = st + act_bytes + q * kWTile;
+              dev::bulk_load(dst, sg, kWTile / 2, full0 + 8 * s, pol_w);
+              dev::bulk_load(dst + kWTile / 2, su, kWTile / 2, full0 + 8 * s, pol_w);
+            }
+          } else {
+            const uint8_t* src =
+                p.w_packed + (static_cast<size_t>(nbf) * p.kb_total + kb) * kWTile;
+            dev::bulk_load(st + act_bytes, src, static_cast<uint32_t>(groups * kWTile),
+                           full0 + 8 * s, pol_w);
+          }
         } else {
           for (int q = 0; q < groups; ++q) {
             const uint8_t* src =
@@ -592,7 +615,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       float wsc[kColsPerThread], wbi[kColsPerThread];
 #pragma unroll
       for (int j = 0; j < kColsPerThread; ++j) {
-        const int n = kSwap ? tn * kTile + row
+        const int n = kSwap ? (p.geglu ? (row < 64 ? 0 : p.f_groups * kTile - 64) + tn * 64 + row
+                                       : tn * kTile + row)
                             : (p.geglu ? (j ? p.f_groups : 0) * kTile + tn * kTile + et
                                        : tn * kBN + et + 128 * j);
         wsc[j] = n < p.N ? (p.w_scale ? __ldg(p.w_scale + n) : 1.0f) : 0.0f;
@@ -618,13 +642,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         dev::named_sync(1, 128);
       } else {
-        const int n = tn * kTile + row;
+        const int n = p.geglu ? (row < 64 ? 0 : p.f_groups * kTile - 64) + tn * 64 + row
+                              : tn * kTile + row;
         if (n < p.N) {
           lcs = as * wsc[0];
           lcb = wbi[0];
-          lact = n < p.act_cols;
+          lact = !p.geglu && n < p.act_cols;
         }
       }
+      // small-M GeGLU: the up lanes (64-127) hand their values to the gate
+      // lanes through shared memory (two alternating buffers of 64 lanes x
+      // 32 floats, one barrier of the epilogue warps per exchange)
+      float* xbuf = reinterpret_cast<float*>(base + p.outbuf_off);
+      auto geglu_rows = [&](float* v, int nv, int buf) -> bool {  // true: this lane stores
+        float* xb = xbuf + buf * (64 * 32);
+        if (row >= 64) {
+          for (int j = 0; j < nv; ++j) xb[j * 64 + (row - 64)] = v[j];
+        }
+        dev::named_sync(1, 128);
+        if (row < 64) {
+          for (int j = 0; j < nv; ++j) v[j] = gelu_tanh(v[j]) * xb[j * 64 + row];
+        }
+        return row < 64;
+      };
       ok = dev::mbar_wait(tfull0 + 8 * b, u & 1, abort_flag, p.dev_status,
                           dev::kTimeoutEpilogue) &&
            scale_ok;
@@ -675,7 +715,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int j = 0; j < 32; ++j) v[j] = gelu_tanh(v[j]);
           }
-          store_rows<32>(v, p, rows_of_tile_m0 + c32, tn * kTile + row);
+          if (!p.geglu)
+            store_rows<32>(v, p, rows_of_tile_m0 + c32, tn * kTile + row);
+          else if (geglu_rows(v, 32, wb))
+            store_rows<32>(v, p, rows_of_tile_m0 + c32, tn * 64 + row);
         }
         wb ^= 1;
       };
@@ -951,7 +994,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
               for (int j = 0; j < 8; ++j) sum[j] = gelu_tanh(sum[j]);
             }
-            store_rows<8>(sum, p, tm * kBN + (own_c0 + lc) * 8, tn * kTile + row);
+            if (!p.geglu)
+              store_rows<8>(sum, p, tm * kBN + (own_c0 + lc) * 8, tn * kTile + row);
+            else if (geglu_rows(sum, 8, lc & 1))
+              store_rows<8>(sum, p, tm * kBN + (own_c0 + lc) * 8, tn * 64 + row);
           }
         } else {
           for (int c = own_c0; c < own_c1; ++c) {
@@ -1057,7 +1103,9 @@ bool layout(Plan& pl, int stage_bytes, int cap = kSmemMax) {
   const int pipe = pl.stages * stage_bytes;
   pl.outbuf_off = pipe;
   pl.recv_off = 0;
-  int tail = pipe + (pl.swap ? 0 : kOutBytes);  // small M stores from registers
+  // small M stores from registers (a GeGLU exchanges its up values through
+  // the same 16 KiB)
+  int tail = pipe + (pl.swap && !pl.geglu ? 0 : kOutBytes);
   if (pl.splits > 1 && !pl.split_global) {
     const int nchunks = pl.bn / pl.chunk_cols;
     const int chunk = kTile * pl.chunk_cols * 4;
@@ -1245,7 +1293,9 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int esize, bool fp8, size_t ws_a
   };
 
   int s_max = 1, g_max = 1;
-  if (pl.num_tiles * ctas_per_tile < sms && !geglu) {  // (a GeGLU tile is finished whole)
+  // (a pair's GeGLU tile is finished whole: its gate and up halves would
+  // meet in different split owners' chunks)
+  if (pl.num_tiles * ctas_per_tile < sms && !(geglu && pl.pair)) {
     s_max = sms / (pl.num_tiles * ctas_per_tile);
     const int nchunks = pl.bn / pl.chunk_cols;
     if (s_max > nchunks) s_max = nchunks;
@@ -1371,7 +1421,7 @@ frt_status gemm_common(bool fp8, const void* a, int64_t lda, const float* a_scal
   const bool geglu = act == FRT_ACT_GEGLU;
   const int64_t n_out = geglu ? N / 2 : N;  // GeGLU: gelu(gate) * up, N / 2 columns
   if (lda < K || ldo < n_out) return FRT_ERR_INVALID_ARG;
-  if (geglu && (M <= 128 || N % 256 != 0)) return FRT_ERR_UNSUPPORTED_SHAPE;
+  if (geglu && N % 256 != 0) return FRT_ERR_UNSUPPORTED_SHAPE;
   if (ldo > (1LL << 31) - 1) return FRT_ERR_UNSUPPORTED_SHAPE;
   if (N % 16 != 0 || K % (fp8 ? 32 : 16) != 0) return FRT_ERR_UNSUPPORTED_SHAPE;
   if (M > (1LL << 31) - 1 || N > (1LL << 31) - 1 || K > (1LL << 31) - 1)

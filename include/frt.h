@@ -225,8 +225,8 @@ frt_status frt_pack_weights(const void* w, frt_dtype w_dtype, int64_t K, int64_t
  * gate and up"): w is [K x N] with the gate's F = N / 2 channels first and
  * the up channels after them (w_scale and bias likewise, N floats), and
  *   out[m, j] = bf16(gelu_tanh(v[m, j]) * v[m, F + j]),  0 <= j < F,
- * so out is [M x F] (ldo >= F); act_cols is ignored.  Requires M > 128 and
- * N % 256 == 0 (else FRT_ERR_UNSUPPORTED_SHAPE).
+ * so out is [M x F] (ldo >= F); act_cols is ignored.  Requires N % 256 == 0
+ * (else FRT_ERR_UNSUPPORTED_SHAPE).
  *
  * a_q / a   : [M x K] row-major, row stride lda; E4M3 OCP bytes (FP8) or
  *             bf16 (BF16); 16-byte aligned, lda * esize a multiple of 16.

@@ -345,7 +345,8 @@ def geglu_oracle(lay, qa_o, sa_o, qw_o, sw_o, kind):
 
 
 @pytest.mark.parametrize("M,K,F", [(300, 1024, 512), (257, 256, 128), (520, 1152, 1280),
-                                   (768, 2048, 16384)])
+                                   (768, 2048, 16384), (50, 1024, 4096), (16, 256, 128),
+                                   (128, 4096, 1024), (1, 512, 256), (64, 2048, 640)])
 @pytest.mark.parametrize("kind", ["e4m3", "bf16"])
 def test_geglu_fused_epilogue(M, K, F, kind):
     # one GEMM over [W_gate, W_up] (2F channels, gate first) whose epilogue
@@ -373,11 +374,6 @@ def test_geglu_fused_epilogue(M, K, F, kind):
 
 
 def test_geglu_rejects_unsupported_shapes():
-    a = torch.zeros((64, 256), dtype=torch.bfloat16, device="cuda")
-    wp = frt.frt_pack_weights(torch.zeros((256, 512), device="cuda"), "bf16")
-    torch.cuda.synchronize()
-    with pytest.raises(frt.FrtError):
-        frt.frt_gemm_bf16(a, wp, 512, geglu=True)  # M <= 128
     a = torch.zeros((300, 256), dtype=torch.bfloat16, device="cuda")
     wp = frt.frt_pack_weights(torch.zeros((256, 384), device="cuda"), "bf16")
     torch.cuda.synchronize()
