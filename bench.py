@@ -599,6 +599,13 @@ def run_components(args, device, sampler, peaks):
             peaks["bf16_tflops_sustained"] * FP8_OVER_BF16)
     out["encoder_gate_up_fp8_m768"] = both
     del gu
+    # the decoder's merged gate/up (1024 -> 2 x 4096) at M=50, BF16 and FP8
+    gu = synth.layer(np.random.default_rng(8), M_DEC, 1024, 2 * 4096, act_cols=4096)
+    for kind in ("bf16", "e4m3"):
+        out["decoder_gate_up_m50_" + ("fp8" if kind == "e4m3" else "bf16")] = {
+            "unfused": gemm_stream_rate(gu, kind, device, sampler),
+            "fused_geglu": gemm_stream_rate(gu, kind, device, sampler, geglu=True)}
+    del gu
     # the encoder FP8 step with each layer's activation scale calibrated once
     # (on that layer's input) and frozen: the quantize is one encode pass
     set0 = EncoderFP8Set(synth.encoder(seed=0, M=M_ENC), device)
