@@ -110,12 +110,18 @@ def aggregate(units_per_rank, seconds_per_rank, world, device=None):
 # ---------------------------------------------------------------- peaks and clocks
 
 def gemm_source_hash():
+    """Hash of the GEMM sources' code: line comments and blank lines are left
+    out, so that editing a comment does not invalidate the recorded ncu
+    figures (the sources hold no '//' inside string literals)."""
     import hashlib
 
     h = hashlib.sha256()
     for f in ("bf16_gemm_vla_gb300/csrc/frt_gemm.cu", "bf16_gemm_vla_gb300/csrc/frt_device.cuh"):
-        with open(os.path.join(ROOT, f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, f), encoding="utf-8") as fh:
+            for line in fh:
+                code = line.split("//", 1)[0].rstrip()
+                if code:
+                    h.update(code.encode() + b"\n")
     return h.hexdigest()[:16]
 
 

@@ -1,5 +1,6 @@
 // FP8 (E4M3 x E4M3, tcgen05 kind::f8f6f4) and BF16 (kind::f16) GEMMs with
-// the fused per-channel-scale + bias (+ tanh-GELU) epilogue and a bf16 store.
+// the fused per-channel-scale + bias (+ tanh-GELU, or the GeGLU of a merged
+// gate/up) epilogue and a bf16 store.
 //
 // The layer computes out = act(acc * a_scale * w_scale[n] + bias[n]) with
 // acc = A[M x K] . W[K x N] in fp32 ("Real-time VLA inference on AMD
@@ -19,8 +20,8 @@
 //   * small M ("swap" tiles): the product is taken transposed,
 //     out^T = W^T . A^T, so the MMA's 128 rows cover output channels and
 //     the few activation rows become the MMA N dimension (32/64/128).  The
-//     weight tile is the operand that streams; every pipeline stage reads a
-//     16 KiB contiguous packed tile.
+//     weight tile is the operand that streams; a pipeline stage reads one
+//     or two contiguous packed 16 KiB k-tiles of a channel group.
 //
 // Both operands are K-major with the 128-byte swizzle.  Activations arrive
 // by TMA (zero fill past M and K); weights are pre-packed into the exact
@@ -44,7 +45,14 @@
 //
 // With programmatic dependent launch, the first pipeline stages' weight
 // tiles (static data) are fetched before the kernel waits for the previous
-// grid; activations and the activation scale are read only after the wait.
+// grid; activations and the activation scale are read only after the wait
+// (the copy warp reads the scale there and hands it to the epilogue through
+// shared memory, so no epilogue waits on an L2 round trip).
+//
+// GeGLU (merged gate/up, gate channels first): a pair tile's CTAs hold the
+// gate group and the matching up group of 128 outputs; a small-M tile's 128
+// weight rows are 64 gate and the 64 matching up channels, and the up lanes
+// hand their values to the gate lanes through shared memory.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
