@@ -273,7 +273,8 @@ size_t frt_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, frt_dtype a_dty
 
 /* The launch plan frt_gemm_fp8 (a_dtype FRT_E4M3_OCP) or frt_gemm_bf16
  * (FRT_BF16) takes for an M x N x K problem given a usable workspace of
- * workspace_bytes bytes, as one line of space-separated key=value fields:
+ * workspace_bytes bytes (with act != FRT_ACT_GEGLU; a GeGLU plan on CTA
+ * pairs never splits K), as one line of space-separated key=value fields:
  *   kind    pair (256-row tiles on CTA pairs) or swap (M <= 128: channels on
  *           the MMA's M side);
  *   bn      tile width (channels for pair, rows for swap);
