@@ -612,6 +612,30 @@ def run_components(args, device, sampler, peaks):
             "unfused": gemm_stream_rate(gu, kind, device, sampler),
             "fused_geglu": gemm_stream_rate(gu, kind, device, sampler, geglu=True)}
     del gu
+    # the BF16 decoder block boundary at M=50, hidden 1024 (gated residual
+    # update + adaptive RMS norm in one launch), back to back over 64 sets
+    H = 1024
+    gen = torch.Generator(device=device)
+    gen.manual_seed(9)
+    bsets = [[(torch.randn((M_DEC, w), generator=gen, device=device) * sd).to(torch.bfloat16)
+              for w, sd in ((H, 1.0), (H, 1.0), (H, 1.0), (3 * H, 0.1))] for _ in range(64)]
+    bouts = [(torch.empty((M_DEC, H), dtype=torch.bfloat16, device=device),
+              torch.empty((M_DEC, H), dtype=torch.bfloat16, device=device)) for _ in bsets]
+
+    def boundary_all():
+        for (res, o, gt, sty), (nrm, nxt) in zip(bsets, bouts):
+            frt.frt_gate_residual_ada_norm_bf16(res, o, gt, sty, normalized=nrm, next_gate=nxt)
+
+    gb = capture(boundary_all)
+    gb.replay()
+    t0 = time.time()
+    secs = device_time(lambda i: gb.replay(), 20) / (20 * len(bsets))
+    sampler.window(t0, time.time())
+    nbytes = M_DEC * H * 2 * (2 + 1 + 1 + 3 + 1 + 1)  # residual r/w, output, gate, style, 2 outputs
+    out["decoder_boundary_m50_h1024"] = {"us": secs * 1e6, "bytes": nbytes,
+                                         "gbs": nbytes / secs / 1e9,
+                                         "note": "latency-bound: 0.9 MB per call, L2-resident"}
+    del gb, bsets, bouts
     # the encoder FP8 step with each layer's activation scale calibrated once
     # (on that layer's input) and frozen: the quantize is one encode pass
     set0 = EncoderFP8Set(synth.encoder(seed=0, M=M_ENC), device)

@@ -11,7 +11,8 @@ the load-time and graph-replay helpers built on it:
 """
 from .frt import (  # noqa: F401
     FNUZ, OCP, PER_COL, PER_TENSOR, FrtError, check_device_status, device_status,
-    frt_fnuz_to_ocp, frt_gemm_bf16, frt_gemm_describe, frt_gemm_fp8, frt_gemm_workspace_bytes,
-    frt_launch_count, frt_pack_weights, frt_packed_weight_bytes, frt_quantize_e4m3, frt_quantize_e4m3_noalloc,
+    frt_fnuz_to_ocp, frt_gate_residual_ada_norm_bf16, frt_gemm_bf16, frt_gemm_describe,
+    frt_gemm_fp8, frt_gemm_workspace_bytes, frt_launch_count, frt_pack_weights,
+    frt_packed_weight_bytes, frt_quantize_e4m3, frt_quantize_e4m3_noalloc,
     frt_quantize_workspace_bytes, gemm_workspace,
 )

@@ -279,3 +279,28 @@ def frt_gemm_bf16(a, w_packed, N, w_scale=None, bias=None, act_cols=0, out=None,
                                M, N, K, act, act_cols, out.data_ptr(), ldo, wp, wb,
                                device_status(a.device).data_ptr(), _stream(stream)))
     return out
+
+
+def frt_gate_residual_ada_norm_bf16(residual, output, gate, style, eps=1e-6, normalized=None,
+                                    next_gate=None, stream=None):
+    """The decoder block boundary: residual <- bf16(residual + output * gate)
+    (in place), normalized = bf16(rms_norm(residual) * (1 + scale) + shift)
+    and next_gate from style = [scale | shift | next gate] ([M x 3H]).  All
+    bf16, contiguous.  Returns (normalized, next_gate)."""
+    M, H = residual.shape
+    for t, shape, name in ((output, (M, H), "output"), (gate, (M, H), "gate"),
+                           (style, (M, 3 * H), "style")):
+        if tuple(t.shape) != shape or t.dtype != torch.bfloat16 or not t.is_contiguous():
+            raise ValueError("%s must be a contiguous bf16 tensor of shape %s" % (name, shape))
+    if residual.dtype != torch.bfloat16 or not residual.is_contiguous():
+        raise ValueError("residual must be a contiguous bf16 tensor")
+    if normalized is None:
+        normalized = torch.empty((M, H), dtype=torch.bfloat16, device=residual.device)
+    if next_gate is None:
+        next_gate = torch.empty((M, H), dtype=torch.bfloat16, device=residual.device)
+    _check("frt_gate_residual_ada_norm_bf16",
+           lib().frt_gate_residual_ada_norm_bf16(residual.data_ptr(), output.data_ptr(),
+                                                 gate.data_ptr(), style.data_ptr(), M, H, eps,
+                                                 normalized.data_ptr(), next_gate.data_ptr(),
+                                                 _stream(stream)))
+    return normalized, next_gate

@@ -302,6 +302,27 @@ frt_status frt_gemm_bf16(const void* a, int64_t lda, const void* w_packed, const
                          int64_t act_cols, void* out, int64_t ldo, void* workspace,
                          size_t workspace_bytes, int* dev_status, frt_stream_t stream);
 
+/* ------------------------------------------------------------------------
+ * The BF16 decoder block boundary in one kernel ("Real-time VLA inference on
+ * AMD hardware", "Fusing the BF16 decoder boundary"), for each row m of an
+ * [M x H] tensor:
+ *   r[m, j]      = bf16(fp32(residual[m, j] + output[m, j] * gate[m, j]))
+ *                  (one fused multiply-add in fp32, then round to bf16)
+ *   inv[m]       = 1 / sqrt(mean_j r[m, j]^2 + eps)                (fp32)
+ *   normalized   = bf16(r * inv * (1 + scale) + shift)
+ *   next_gate    = gate part of style
+ * style is [M x 3H]: scale in columns [0, H), shift in [H, 2H), the next
+ * block's gate in [2H, 3H) (the page names the steps, not this layout: it is
+ * a reading).  residual is updated in place to r.  All tensors bf16,
+ * row-major and contiguous, 16-byte aligned; normalized and next_gate are
+ * [M x H] outputs.  Requires H % 8 == 0 and H <= 4096 (else
+ * FRT_ERR_UNSUPPORTED_SHAPE), eps >= 0.  M == 0 enqueues nothing.  Legal
+ * under stream capture; allocates nothing.
+ * ---------------------------------------------------------------------- */
+frt_status frt_gate_residual_ada_norm_bf16(void* residual, const void* output, const void* gate,
+                                           const void* style, int64_t M, int64_t H, float eps,
+                                           void* normalized, void* next_gate, frt_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -140,3 +140,16 @@ def test_gemm_rejects_bad_arguments(lib):
              None) == 2
     assert b(FAKE, 1028, FAKE, None, None, 50, 1024, 1024, 0, 0, FAKE, 1024, None, 0, None,
              None) == 3
+
+
+def test_decoder_boundary_rejects_bad_arguments(lib):
+    f = lib.frt_gate_residual_ada_norm_bf16
+    code = {name: c for c, name in _lib.STATUS_NAMES.items()}
+    ok = [FAKE, FAKE, FAKE, FAKE, 50, 1024, 1e-6, FAKE, FAKE, None]
+    assert f(*ok[:4], 0, 1024, 1e-6, *ok[7:]) == code["FRT_OK"]  # M = 0: nothing
+    for i, v, want in ((4, -1, "FRT_ERR_INVALID_ARG"), (5, 12, "FRT_ERR_UNSUPPORTED_SHAPE"),
+                       (5, 4104, "FRT_ERR_UNSUPPORTED_SHAPE"), (6, -1.0, "FRT_ERR_INVALID_ARG"),
+                       (0, None, "FRT_ERR_INVALID_ARG"), (3, FAKE + 8, "FRT_ERR_MISALIGNED")):
+        a = list(ok)
+        a[i] = v
+        assert f(*a) == code[want], (i, v)
