@@ -59,3 +59,25 @@ def test_peaks_fall_back_without_measurements(tmp_path, monkeypatch):
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     peaks, kind = bench.load_peaks()
     assert kind == "fallback" and peaks["hbm_gbs"] == 6800.0
+
+
+def test_profiled_traffic_keyed_to_gemm_code_not_comments(tmp_path, monkeypatch):
+    # the recorded ncu DRAM figures apply while the GEMM sources' code is the
+    # captured one: a comment edit keeps them, a code edit drops them (null)
+    csrc = tmp_path / "bf16_gemm_vla_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    for f in ("frt_gemm.cu", "frt_device.cuh"):
+        (csrc / f).write_text("int x = 1;  // a comment\n\n// another\nint y = 2;\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    h = bench.gemm_source_hash()
+    (prof / "gemm_fp8_dram_traffic.txt").write_text(
+        "# header\nsource %s\n768 2048 16384 100\n768 16384 2048 300\n" % h)
+    shapes = [(768, 2048, 16384), (768, 16384, 2048)]
+    assert bench.profiled_traffic(shapes) == 200.0
+    (csrc / "frt_gemm.cu").write_text("int x = 1;  // the comment, reworded\nint y = 2;\n")
+    assert bench.gemm_source_hash() == h and bench.profiled_traffic(shapes) == 200.0
+    (csrc / "frt_gemm.cu").write_text("int x = 3;\nint y = 2;\n")
+    assert bench.gemm_source_hash() != h and bench.profiled_traffic(shapes) is None
+    assert bench.profiled_traffic([(1, 2, 3)]) is None  # a shape without a figure
