@@ -109,18 +109,30 @@ class Linear:
         self.static = True
         return best
 
-    def __call__(self, x, stream=None):
+    def quantize(self, x, stream=None):
+        """FP8 layers: the activation quantize of x into self.q / self.a_scale
+        (nothing for BF16 layers)."""
+        if self.w.kind != "e4m3":
+            return
+        if self.static:
+            frt.frt_quantize_e4m3(x, frt.PER_TENSOR, frt.OCP, static_scale=self.a_scale,
+                                  q=self.q, scale=self.s_out, stream=stream)
+        else:
+            frt.frt_quantize_e4m3(x, frt.PER_TENSOR, frt.OCP, q=self.q, scale=self.a_scale,
+                                  workspace=self.ws, stream=stream)
+
+    def gemm(self, x, stream=None):
+        """The GEMM alone: FP8 layers read self.q / self.a_scale (x unused),
+        BF16 layers read x."""
         w = self.w
         if w.kind == "e4m3":
-            if self.static:
-                frt.frt_quantize_e4m3(x, frt.PER_TENSOR, frt.OCP, static_scale=self.a_scale,
-                                      q=self.q, scale=self.s_out, stream=stream)
-            else:
-                frt.frt_quantize_e4m3(x, frt.PER_TENSOR, frt.OCP, q=self.q, scale=self.a_scale,
-                                      workspace=self.ws, stream=stream)
             return frt.frt_gemm_fp8(self.q, self.a_scale, w.packed, w.w_scale, w.N, bias=w.bias,
                                     act_cols=self.act_cols, out=self.out, stream=stream,
                                     workspace=self.gws, geglu=self.geglu)
         return frt.frt_gemm_bf16(x, w.packed, w.N, w_scale=w.w_scale, bias=w.bias,
                                  act_cols=self.act_cols, out=self.out, stream=stream,
                                  workspace=self.gws, geglu=self.geglu)
+
+    def __call__(self, x, stream=None):
+        self.quantize(x, stream)
+        return self.gemm(x, stream)

@@ -36,14 +36,17 @@ M_DEC = 50
 
 class SyntheticStack:
     def __init__(self, n_layers=18, seed=1, device="cuda", enc_kind="e4m3", dec_kind="bf16",
-                 keep=(0, 17)):
+                 keep=(0, 17), parts=("enc", "dec")):
+        """parts: the chains to build ("enc", "dec" or both); a chain left out
+        is empty and its weights are not drawn (the other chain's draws are
+        then not those of the full stack)."""
         self.device = torch.device(device)
         self.n_layers = n_layers
         g = torch.Generator(device=self.device)
         g.manual_seed(seed)
         self.kept = {}  # (part, layer, name) -> (w fp32 cpu, bias fp32 cpu)
-        self.enc = self._build("enc", ENCODER, M_ENC, enc_kind, g, keep)
-        self.dec = self._build("dec", DECODER, M_DEC, dec_kind, g, keep)
+        self.enc = self._build("enc", ENCODER, M_ENC, enc_kind, g, keep) if "enc" in parts else []
+        self.dec = self._build("dec", DECODER, M_DEC, dec_kind, g, keep) if "dec" in parts else []
         self.x_enc = torch.zeros((M_ENC, ENCODER[0][1]), dtype=torch.bfloat16, device=self.device)
         self.x_dec = torch.zeros((M_DEC, DECODER[0][1]), dtype=torch.bfloat16, device=self.device)
         self.graph = None
@@ -71,6 +74,24 @@ class SyntheticStack:
             gu = lay["gate_up"](o, stream)
             x = lay["down"](gu[:, : lay["down"].w.K], stream)
         return x
+
+    def op_list(self):
+        """Every launch of one forward in order, as (part, layer, name, op,
+        lin, call): op is "quantize" (FP8 layers only) or "gemm", lin the
+        layer's Linear, and call(stream) enqueues the launch on the buffers
+        the forward uses."""
+        ops = []
+        for part, chain in (("enc", self.enc), ("dec", self.dec)):
+            for li, lay in enumerate(chain):
+                for name in ("qkv", "o", "gate_up", "down"):
+                    lin = lay[name]
+                    x = self.inputs_of(part, li, name)
+                    if lin.w.kind == "e4m3":
+                        ops.append((part, li, name, "quantize", lin,
+                                    lambda s=None, lin=lin, x=x: lin.quantize(x, s)))
+                    ops.append((part, li, name, "gemm", lin,
+                                lambda s=None, lin=lin, x=x: lin.gemm(x, s)))
+        return ops
 
     def inputs_of(self, part, li, name):
         """The activation tensor layer (part, li, name) reads, after a forward."""

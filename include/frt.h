@@ -123,9 +123,13 @@ const char* frt_status_string(frt_status status);
  *             both passes: each CTA holds its part of x, the CTAs meet at a
  *             barrier in the header (so the grid's CTAs, at most one per SM,
  *             must all be resident at once), and x is read once.  A CTA that
- *             waits there for over a second gives up: the call's scale
- *             becomes NaN and header word 1 (bytes 4-7) nonzero; the
- *             caller then zero-fills the header again.
+ *             waits there for over a second gives up: its part of q is NaN
+ *             codes (and s is NaN if that CTA is the first, which writes
+ *             it), and header word 1 (bytes 4-7) becomes nonzero (a record for the caller; no kernel reads
+ *             it).  Every CTA still arrives at the barrier, so once all the
+ *             call's CTAs have finished the header is ready for the next
+ *             call again.  Only a header whose words were written by
+ *             something other than these kernels needs zero-filling again.
  * Requires rows, cols >= 0, ldx >= cols; x, q, scale 4-byte aligned.
  * Vector paths are taken when x/q are 16-byte aligned and cols, ldx are
  * multiples of 8; other shapes take a scalar path with the same results.
@@ -161,10 +165,10 @@ frt_status frt_quantize_e4m3(const void* x, frt_dtype x_dtype, int64_t rows, int
  *   - All calls share the one array, and each call overwrites the partials
  *     it reads and leaves the header ready for the next call, so nothing needs
  *     clearing between calls; calls that overlap on the GPU (different
- *     streams, no ordering) race on it.  After a one-grid call that gave up
- *     (NaN scale, see frt_quantize_e4m3) the header is not restored and
- *     later per-tensor calls on that device are invalid until the process
- *     restarts.
+ *     streams, no ordering) race on it.  A one-grid call that gave up at
+ *     its barrier (NaN scale and NaN codes, see frt_quantize_e4m3) still
+ *     leaves the header ready for the next call once all its CTAs have
+ *     finished (header word 1 keeps the give-up record; no kernel reads it).
  * ---------------------------------------------------------------------- */
 frt_status frt_quantize_e4m3_noalloc(const void* x, frt_dtype x_dtype, int64_t rows, int64_t cols,
                                      int64_t ldx, frt_scale_mode mode, frt_dtype out_fmt,
