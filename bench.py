@@ -883,15 +883,17 @@ def stack_kernel_table(st, sampler, peaks, replay_secs):
         M, K, N = lin.M, lin.w.K, lin.w.N
         row = {"chain": part, "layer": name, "op": op, "M": M, "K": K, "N": N,
                "launches": len(items), "us": per * 1e6}
-        if op == "quantize":
-            row["kernel"] = "quantize (per tensor, dynamic)"
+        if op in ("quantize", "encode"):
+            row["kernel"] = ("quantize (per tensor, dynamic)" if op == "quantize" else
+                             "quantize encode pass (per tensor, scale taken by the GEMM before)")
             row["gbs_3B_per_elem"] = 3.0 * M * K / per / 1e9
             row["bound"] = "hbm"
             row["frac"] = row["gbs_3B_per_elem"] / hbm
         else:
             pl = frt.frt_gemm_describe(M, N, K, lin.w.kind)
-            row["kernel"] = "gemm_tc_kernel<%s, %s, %d>" % (
-                "fp8" if lin.w.kind == "e4m3" else "bf16", pl["kind"], pl["bn"])
+            row["kernel"] = "gemm_tc_kernel<%s, %s, %d>%s" % (
+                "fp8" if lin.w.kind == "e4m3" else "bf16", pl["kind"], pl["bn"],
+                " taking the next layer's scale" if op == "gemm+scale" else "")
             row["tflops"] = 2.0 * M * N * K / per / 1e12
             row["weight_gbs"] = lin.w.packed.numel() / per / 1e9
             if M > 128:

@@ -47,6 +47,13 @@ SIGNATURES = {
     "frt_gemm_workspace_bytes": (_c_sz, [_c_i64, _c_i64, _c_i64, _c_int]),
     "frt_gemm_describe": (_c_int, [_c_i64, _c_i64, _c_i64, _c_int, _c_sz, ctypes.c_char_p,
                                    _c_sz]),
+    "frt_gemm_next_scale_workspace_bytes": (_c_sz, []),
+    "frt_gemm_fp8_next_scale": (_c_int, [_c_p, _c_i64, _c_p, _c_p, _c_p, _c_p, _c_i64, _c_i64,
+                                         _c_i64, _c_int, _c_i64, _c_p, _c_i64, _c_i64, _c_p, _c_p,
+                                         _c_sz, _c_p, _c_sz, _c_p, _c_p]),
+    "frt_gemm_bf16_next_scale": (_c_int, [_c_p, _c_i64, _c_p, _c_p, _c_p, _c_i64, _c_i64, _c_i64,
+                                          _c_int, _c_i64, _c_p, _c_i64, _c_i64, _c_p, _c_p, _c_sz,
+                                          _c_p, _c_sz, _c_p, _c_p]),
     "frt_gate_residual_ada_norm_bf16": (_c_int, [_c_p, _c_p, _c_p, _c_p, _c_i64, _c_i64,
                                                  ctypes.c_float, _c_p, _c_p, _c_p]),
     "frt_gemm_fp8": (_c_int, [_c_p, _c_i64, _c_p, _c_p, _c_p, _c_p, _c_i64, _c_i64, _c_i64,

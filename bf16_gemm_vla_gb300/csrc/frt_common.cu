@@ -28,7 +28,7 @@ void note_launches(int n) { g_launches.fetch_add(static_cast<unsigned long long>
 
 }  // namespace frt
 
-extern "C" int frt_abi_version(void) { return 2; }
+extern "C" int frt_abi_version(void) { return 3; }
 
 extern "C" unsigned long long frt_launch_count(void) { return frt::g_launches.load(); }
 

@@ -14,6 +14,7 @@ enum : int {
   kTimeoutProducer = 0x101,
   kTimeoutMma = 0x102,
   kTimeoutEpilogue = 0x103,
+  kTimeoutQuantOut = 0x104,  // the grid barrier of a GEMM's fused output quantize
 };
 
 // A wait gives up after this many nanoseconds of %globaltimer.

@@ -62,6 +62,7 @@
 #include <mutex>
 
 #include "frt_device.cuh"
+#include "frt_e4m3.cuh"
 #include "frt_host.h"
 
 namespace frt {
@@ -78,6 +79,7 @@ constexpr int kOutBytes = 4 * 2 * kWarpOutBytes;  // 4 epilogue warps x 2 buffer
 constexpr int kBarRegion = 512;          // mbarriers, TMEM address, abort flag
 constexpr int kMaxSplits = 8;            // portable cluster size
 constexpr int kMaxStages = 8;
+constexpr size_t kNextScaleHeaderBytes = 256;  // arrivals and running max of the next layer's scale
 
 struct GemmArgs {
   const uint8_t* w_packed;
@@ -111,6 +113,12 @@ struct GemmArgs {
   float* ws_part;      // split_global: partial chunks, one slot per (tile, CTA, chunk, split)
   unsigned* ws_flag;   // split_global: per (tile, CTA, owner split) arrival counters
   int* dev_status;
+  // The next FP8 layer's activation scale, taken from this layer's own bf16
+  // output (s_cols 0: not asked for): s = amax / 448 over out[0:M, 0:s_cols]
+  // (NaN ignored; 1 if the amax is 0), folded across the CTAs in s_hdr.
+  int s_cols;
+  float* s_out;    // receives s
+  unsigned* s_hdr; // 256-byte header: [0] arrivals, [4] running max (fp32 bits)
 };
 
 template <bool kSwap, bool kPair, int kBN>
@@ -212,6 +220,81 @@ __device__ __forceinline__ uint32_t chunk_off(int r, int q, int cw) {
   return static_cast<uint32_t>(r * cw * 4 + ((q ^ swz) << 4));
 }
 
+// ------------------------------------------------------------------ the next layer's scale
+//
+// The per-tensor E4M3 scale of the layer's own bf16 output, for the next FP8
+// layer, taken in the epilogue instead of by a separate amax pass over the
+// stored output: each epilogue thread keeps the running max |bf16(v)| of the
+// outputs it stores in the first s_cols columns, each CTA folds its maximum
+// into a header word after its last tile and arrives on an arrival count;
+// the last CTA to arrive turns the maximum into s = amax / 448 (1 if 0),
+// stores it and resets the header.  No CTA waits for another.  The encode
+// with s is then the static-scale quantize of the stored output (a light
+// pass over the output, which is still in L2).
+
+__device__ __forceinline__ float bf16_round(float v) {
+  return __bfloat162float(__float2bfloat16_rn(v));
+}
+
+// max |x| over the 8 bf16 values of a 16-byte vector and a running bf16x2
+// maximum (sign bits cleared; a NaN operand of __hmax2 yields the other
+// one, as fmaxf: NaN is ignored).
+__device__ __forceinline__ uint32_t max_abs_bf16x8(uint32_t acc, const uint4& w) {
+  __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&acc);
+  const uint32_t ws[4] = {w.x & 0x7FFF7FFFu, w.y & 0x7FFF7FFFu, w.z & 0x7FFF7FFFu,
+                          w.w & 0x7FFF7FFFu};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) a = __hmax2(a, *reinterpret_cast<const __nv_bfloat162*>(&ws[k]));
+  return *reinterpret_cast<const uint32_t*>(&a);
+}
+
+// Large M: the running max over this thread's 32 bf16 outputs of row m,
+// columns n0 .. n0 + 31 (n0 a multiple of 32; s_cols a multiple of 8), read
+// back from the row the thread staged for the TMA store (64 bytes, 16-byte
+// chunk c at c ^ sw): the stored values.
+__device__ __forceinline__ void amax_row32_staged(const GemmArgs& p, float& amax,
+                                                  const uint8_t* rowp, int sw, int m, int n0) {
+  if (m >= p.M || n0 >= p.s_cols) return;
+  const int nc = min(4, (p.s_cols - n0) >> 3);  // 8-column vectors inside s_cols
+  uint32_t m2 = 0u;
+#pragma unroll
+  for (int c = 0; c < 4; ++c)
+    if (c < nc) m2 = max_abs_bf16x8(m2, *reinterpret_cast<const uint4*>(rowp + ((c ^ sw) << 4)));
+  amax = fmaxf(amax, fmaxf(__uint_as_float(m2 << 16), __uint_as_float(m2 & 0xFFFF0000u)));
+}
+
+// Small M: the running max over the bf16 outputs of channel n for rows
+// y0 .. y0 + kRows - 1.
+template <int kRows>
+__device__ __forceinline__ void amax_col(const GemmArgs& p, float& amax, const float* v, int y0,
+                                         int n) {
+  if (n >= p.s_cols) return;
+#pragma unroll
+  for (int j = 0; j < kRows; ++j)
+    if (y0 + j < p.M) amax = fmaxf(amax, fabsf(bf16_round(v[j])));
+}
+
+// One thread per CTA, after the CTA's last output: folds the CTA's maximum m
+// into the header and arrives; the last arrival stores s and resets the
+// header for the next call.
+__device__ __noinline__ void next_scale_arrive(const GemmArgs& p, float m) {
+  unsigned* hdr = p.s_hdr;
+  const unsigned nct = gridDim.x * gridDim.y * gridDim.z;
+  // the header's previous user (an earlier grid on the stream) has completed
+  dev::grid_dependency_wait();
+  // m >= 0 and never NaN: its bits order as its value.  The running maximum
+  // only grows within a call, so a CTA whose maximum is not above the value
+  // it reads skips the atomic (fewer operations on the contended line).
+  if (__uint_as_float(ld_relaxed_gpu(hdr + 4)) < m) atomicMax(hdr + 4, __float_as_uint(m));
+  // the arrival releases this CTA's maximum; the last one acquires them all
+  if (atom_add_acq_rel_gpu(hdr, 1u) == nct - 1) {
+    const float a = __uint_as_float(ld_relaxed_gpu(hdr + 4));
+    hdr[4] = 0u;
+    hdr[0] = 0u;
+    *p.s_out = a == 0.0f ? 1.0f : __fdiv_rn(a, 448.0f);
+  }
+}
+
 template <bool kFp8, bool kSwap, bool kPair, int kBN>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_act,
@@ -240,6 +323,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * stages + 6);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float* a_scale_s = reinterpret_cast<float*>(tmem_slot + 2);
+  float* amax_red = a_scale_s + 1;  // the epilogue warps' output maxima (next layer's scale)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -600,6 +684,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int wb = 0;
     bool ok = true;
     bool bye = false;  // arrived on the pair's final cluster barrier
+    float amax = 0.0f;  // running max |bf16 output| in the first s_cols columns
     // a drained accumulator buffer goes back to the MMA issuer (the leader
     // of a pair, whose MMAs write both CTAs' TMEM)
     auto release_acc = [&](int b) {
@@ -716,6 +801,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           warp_store<false, 32>(v, wbuf + wb * kWarpOutBytes, wbuf_s + wb * kWarpOutBytes,
                                 &tmap_out, n0, row0 + ew * 32, lane);
+          if (p.s_cols)
+            amax_row32_staged(p, amax, wbuf + wb * kWarpOutBytes + lane * 64, (lane >> 1) & 3,
+                           row0 + ew * 32 + lane, n0);
         } else {
 #pragma unroll
           for (int j = 0; j < 32; ++j) v[j] = lin(v[j], lcs, lcb);
@@ -723,10 +811,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int j = 0; j < 32; ++j) v[j] = gelu_tanh(v[j]);
           }
-          if (!p.geglu)
+          if (!p.geglu) {
+            if (p.s_cols) amax_col<32>(p, amax, v, rows_of_tile_m0 + c32, tn * kTile + row);
             store_rows<32>(v, p, rows_of_tile_m0 + c32, tn * kTile + row);
-          else if (geglu_rows(v, 32, wb))
+          } else if (geglu_rows(v, 32, wb)) {
+            if (p.s_cols) amax_col<32>(p, amax, v, rows_of_tile_m0 + c32, tn * 64 + row);
             store_rows<32>(v, p, rows_of_tile_m0 + c32, tn * 64 + row);
+          }
         }
         wb ^= 1;
       };
@@ -756,6 +847,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             warp_store<false, 32>(g, wbuf + wb * kWarpOutBytes, wbuf_s + wb * kWarpOutBytes,
                                   &tmap_out, tn * kTile + c, row0 + ew * 32, lane);
+            if (p.s_cols)
+              amax_row32_staged(p, amax, wbuf + wb * kWarpOutBytes + lane * 64, (lane >> 1) & 3,
+                             row0 + ew * 32 + lane, tn * kTile + c);
             wb ^= 1;
           }
           }
@@ -1002,10 +1096,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
               for (int j = 0; j < 8; ++j) sum[j] = gelu_tanh(sum[j]);
             }
-            if (!p.geglu)
+            if (!p.geglu) {
+              if (p.s_cols) amax_col<8>(p, amax, sum, tm * kBN + (own_c0 + lc) * 8, tn * kTile + row);
               store_rows<8>(sum, p, tm * kBN + (own_c0 + lc) * 8, tn * kTile + row);
-            else if (geglu_rows(sum, 8, lc & 1))
+            } else if (geglu_rows(sum, 8, lc & 1)) {
+              if (p.s_cols) amax_col<8>(p, amax, sum, tm * kBN + (own_c0 + lc) * 8, tn * 64 + row);
               store_rows<8>(sum, p, tm * kBN + (own_c0 + lc) * 8, tn * 64 + row);
+            }
           }
         } else {
           for (int c = own_c0; c < own_c1; ++c) {
@@ -1041,6 +1138,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (early_bye && !bye) dev::cluster_arrive_relaxed();
     if (lane == 0) dev::bulk_wait_all();  // stores complete before the grid ends
+    if (p.s_cols) {
+      // the next layer's scale: the CTA's maximum, folded in by one thread
+      float m = amax;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+      if (lane == 0) amax_red[warp - 2] = m;
+      dev::named_sync(1, 128);
+      if (et == 0)
+        next_scale_arrive(p, fmaxf(fmaxf(amax_red[0], amax_red[1]),
+                                   fmaxf(amax_red[2], amax_red[3])));
+    }
   }
 
   if (csplit) {
@@ -1368,7 +1476,12 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int esize, bool fp8, size_t ws_a
     pl.grid = dim3(static_cast<unsigned>(pl.num_tiles * ctas_per_tile), 1,
                    static_cast<unsigned>(pl.splits));
   } else {
-    const int units = sms / ctas_per_tile;  // persistent: one CTA (pair) per SM (two SMs)
+    // persistent: one CTA (pair) per SM (two SMs), and no more CTAs (pairs)
+    // than can be resident at once, so that the grid is one wave
+    int units = sms / ctas_per_tile;
+    const int cap = fp8 ? cluster_capacity_for<true>(pl, 1, pl.smem)
+                        : cluster_capacity_for<false>(pl, 1, pl.smem);
+    if (cap > 0 && cap < units) units = cap;
     pl.grid = dim3(static_cast<unsigned>((pl.num_tiles < units ? pl.num_tiles : units) *
                                          ctas_per_tile),
                    1, 1);
@@ -1414,11 +1527,19 @@ cudaError_t dispatch(const CUtensorMap& ta, const CUtensorMap& tw, const CUtenso
   }
 }
 
+// The next layer's scale taken in a GEMM's epilogue (none when scale is null).
+struct NextScale {
+  int64_t cols;
+  float* scale;
+  void* hdr;
+  size_t hdr_bytes;
+};
+
 frt_status gemm_common(bool fp8, const void* a, int64_t lda, const float* a_scale,
                        const void* w_packed, const float* w_scale, const float* bias, int64_t M,
                        int64_t N, int64_t K, frt_act act, int64_t act_cols, void* out,
                        int64_t ldo, void* workspace, size_t workspace_bytes, int* dev_status,
-                       frt_stream_t stream) {
+                       frt_stream_t stream, const NextScale& ns = NextScale{}) {
   const int esize = fp8 ? 1 : 2;
   if (!a || !w_packed || !out) return FRT_ERR_INVALID_ARG;
   if (fp8 && (!a_scale || !w_scale)) return FRT_ERR_INVALID_ARG;
@@ -1440,6 +1561,12 @@ frt_status gemm_common(bool fp8, const void* a, int64_t lda, const float* a_scal
   if ((a_scale && !aligned(a_scale, 4)) || (w_scale && !aligned(w_scale, 4)) ||
       (bias && !aligned(bias, 4)) || (dev_status && !aligned(dev_status, 4)))
     return FRT_ERR_MISALIGNED;
+  if (ns.scale) {
+    if (ns.cols < 1 || ns.cols > n_out || !ns.hdr) return FRT_ERR_INVALID_ARG;
+    if (ns.cols % 8 != 0) return FRT_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned(ns.scale, 4) || !aligned(ns.hdr, 16)) return FRT_ERR_MISALIGNED;
+    if (ns.hdr_bytes < kNextScaleHeaderBytes) return FRT_ERR_WORKSPACE_TOO_SMALL;
+  }
 
   const int64_t kb_total = ceil_div(K * esize, kKBytes);
   const int64_t nb_total = ceil_div(N, kTile);
@@ -1544,6 +1671,9 @@ frt_status gemm_common(bool fp8, const void* a, int64_t lda, const float* a_scal
                    ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + pl.ws_flag_bytes)
                    : nullptr;
   ga.dev_status = dev_status;
+  ga.s_cols = ns.scale ? static_cast<int>(ns.cols) : 0;
+  ga.s_out = ns.scale;
+  ga.s_hdr = ns.scale ? static_cast<unsigned*>(ns.hdr) : nullptr;
 
   cudaError_t e = fp8 ? dispatch<true>(ta, tw, to, ga, pl, as_cuda(stream))
                       : dispatch<false>(ta, tw, to, ga, pl, as_cuda(stream));
@@ -1583,6 +1713,33 @@ extern "C" frt_status frt_gemm_bf16(const void* a, int64_t lda, const void* w_pa
                                     int* dev_status, frt_stream_t stream) {
   return frt::gemm_common(false, a, lda, nullptr, w_packed, w_scale, bias, M, N, K, act, act_cols,
                           out, ldo, workspace, workspace_bytes, dev_status, stream);
+}
+
+extern "C" size_t frt_gemm_next_scale_workspace_bytes(void) {
+  return frt::kNextScaleHeaderBytes;
+}
+
+extern "C" frt_status frt_gemm_fp8_next_scale(
+    const uint8_t* a_q, int64_t lda, const float* a_scale, const void* w_packed,
+    const float* w_scale, const float* bias, int64_t M, int64_t N, int64_t K, frt_act act,
+    int64_t act_cols, void* out, int64_t ldo, int64_t scale_cols, float* scale,
+    void* scale_workspace, size_t scale_workspace_bytes, void* workspace, size_t workspace_bytes,
+    int* dev_status, frt_stream_t stream) {
+  if (!scale) return FRT_ERR_INVALID_ARG;
+  const frt::NextScale ns = {scale_cols, scale, scale_workspace, scale_workspace_bytes};
+  return frt::gemm_common(true, a_q, lda, a_scale, w_packed, w_scale, bias, M, N, K, act,
+                          act_cols, out, ldo, workspace, workspace_bytes, dev_status, stream, ns);
+}
+
+extern "C" frt_status frt_gemm_bf16_next_scale(
+    const void* a, int64_t lda, const void* w_packed, const float* w_scale, const float* bias,
+    int64_t M, int64_t N, int64_t K, frt_act act, int64_t act_cols, void* out, int64_t ldo,
+    int64_t scale_cols, float* scale, void* scale_workspace, size_t scale_workspace_bytes,
+    void* workspace, size_t workspace_bytes, int* dev_status, frt_stream_t stream) {
+  if (!scale) return FRT_ERR_INVALID_ARG;
+  const frt::NextScale ns = {scale_cols, scale, scale_workspace, scale_workspace_bytes};
+  return frt::gemm_common(false, a, lda, nullptr, w_packed, w_scale, bias, M, N, K, act, act_cols,
+                          out, ldo, workspace, workspace_bytes, dev_status, stream, ns);
 }
 
 extern "C" int frt_gemm_describe(int64_t M, int64_t N, int64_t K, frt_dtype a_dtype,

@@ -281,6 +281,67 @@ def frt_gemm_bf16(a, w_packed, N, w_scale=None, bias=None, act_cols=0, out=None,
     return out
 
 
+def frt_gemm_next_scale_workspace_bytes():
+    return lib().frt_gemm_next_scale_workspace_bytes()
+
+
+def next_scale_workspace(device=None):
+    """A zero-filled header for the next layer's scale taken by a GEMM."""
+    return torch.zeros((frt_gemm_next_scale_workspace_bytes(),), dtype=torch.uint8, device=device)
+
+
+def _next_scale(out, scale_cols, scale, scale_workspace):
+    if scale_cols is None:
+        scale_cols = out.shape[1]
+    if scale is None:
+        scale = torch.empty((1,), dtype=torch.float32, device=out.device)
+    if scale_workspace is None:
+        scale_workspace = next_scale_workspace(out.device)
+    return (scale_cols, scale, scale_workspace.data_ptr(),
+            scale_workspace.numel() * scale_workspace.element_size())
+
+
+def frt_gemm_fp8_next_scale(a_q, a_scale, w_packed, w_scale, N, bias=None, act_cols=0, out=None,
+                            scale_cols=None, scale=None, scale_workspace=None, stream=None,
+                            workspace=None, geglu=False):
+    """frt_gemm_fp8 that also writes the per-tensor OCP E4M3 scale of its own
+    bf16 output out[:, :scale_cols] (amax / 448) for the next FP8 layer,
+    whose quantize is then frt_quantize_e4m3(out[:, :scale_cols],
+    static_scale=scale).  Returns (out, scale).  scale_workspace: a
+    zero-filled header (shared only by calls ordered on one stream;
+    allocated when not given)."""
+    M, K, lda = _rows_view(a_q, "a_q")
+    out, ldo = _gemm_out(M, N // 2 if geglu else N, out, a_q.device)
+    cols, scale, sw, swb = _next_scale(out, scale_cols, scale, scale_workspace)
+    act, act_cols = _act(act_cols, geglu)
+    wp, wb = _gemm_ws(workspace, M, N, K, "e4m3", a_q.device)
+    _check("frt_gemm_fp8_next_scale",
+           lib().frt_gemm_fp8_next_scale(a_q.data_ptr(), lda, _ptr(a_scale), w_packed.data_ptr(),
+                                         _ptr(w_scale), _ptr(bias), M, N, K, act, act_cols,
+                                         out.data_ptr(), ldo, cols, scale.data_ptr(), sw, swb,
+                                         wp, wb, device_status(a_q.device).data_ptr(),
+                                         _stream(stream)))
+    return out, scale
+
+
+def frt_gemm_bf16_next_scale(a, w_packed, N, w_scale=None, bias=None, act_cols=0, out=None,
+                             scale_cols=None, scale=None, scale_workspace=None, stream=None,
+                             workspace=None, geglu=False):
+    """frt_gemm_bf16 that also writes the next FP8 layer's scale (as
+    frt_gemm_fp8_next_scale).  Returns (out, scale)."""
+    M, K, lda = _rows_view(a, "a")
+    out, ldo = _gemm_out(M, N // 2 if geglu else N, out, a.device)
+    cols, scale, sw, swb = _next_scale(out, scale_cols, scale, scale_workspace)
+    act, act_cols = _act(act_cols, geglu)
+    wp, wb = _gemm_ws(workspace, M, N, K, "bf16", a.device)
+    _check("frt_gemm_bf16_next_scale",
+           lib().frt_gemm_bf16_next_scale(a.data_ptr(), lda, w_packed.data_ptr(), _ptr(w_scale),
+                                          _ptr(bias), M, N, K, act, act_cols, out.data_ptr(), ldo,
+                                          cols, scale.data_ptr(), sw, swb, wp, wb,
+                                          device_status(a.device).data_ptr(), _stream(stream)))
+    return out, scale
+
+
 def frt_gate_residual_ada_norm_bf16(residual, output, gate, style, eps=1e-6, normalized=None,
                                     next_gate=None, stream=None):
     """The decoder block boundary: residual <- bf16(residual + output * gate)

@@ -85,6 +85,9 @@ class Linear:
             self.ws = torch.zeros((max(nb, 4) // 4,), dtype=torch.float32, device=dev)
             self.static = False
             self.s_out = torch.empty((1,), dtype=torch.float32, device=dev)  # static path's copy
+            # header for a previous GEMM that takes this layer's activation
+            # scale from its own output (zero-filled once)
+            self.sws = frt.next_scale_workspace(dev)
         # the GEMM's own (zero-filled) workspace, or False if it needs none
         gws = frt.gemm_workspace(M, weight.N, weight.K, weight.kind, dev)
         self.gws = False if gws is None else gws
@@ -109,22 +112,40 @@ class Linear:
         self.static = True
         return best
 
-    def quantize(self, x, stream=None):
+    def quantize(self, x, stream=None, scale_ready=False):
         """FP8 layers: the activation quantize of x into self.q / self.a_scale
-        (nothing for BF16 layers)."""
+        (nothing for BF16 layers).  scale_ready: the GEMM that produced x has
+        written x's scale into self.a_scale already, so this is the encode
+        pass alone."""
         if self.w.kind != "e4m3":
             return
-        if self.static:
+        if self.static or scale_ready:
             frt.frt_quantize_e4m3(x, frt.PER_TENSOR, frt.OCP, static_scale=self.a_scale,
                                   q=self.q, scale=self.s_out, stream=stream)
         else:
             frt.frt_quantize_e4m3(x, frt.PER_TENSOR, frt.OCP, q=self.q, scale=self.a_scale,
                                   workspace=self.ws, stream=stream)
 
-    def gemm(self, x, stream=None):
+    def gemm(self, x, stream=None, next_layer=None):
         """The GEMM alone: FP8 layers read self.q / self.a_scale (x unused),
-        BF16 layers read x."""
+        BF16 layers read x.  next_layer: an FP8 Linear with a dynamic scale
+        whose input is the first next_layer.w.K columns of this layer's
+        output; the GEMM then also writes that input's scale into
+        next_layer.a_scale (taken in its epilogue), and next_layer's quantize
+        is called with scale_ready=True."""
         w = self.w
+        if next_layer is not None:
+            nl = next_layer
+            if nl.w.kind != "e4m3" or nl.static:
+                raise ValueError("the next layer's scale is taken for an FP8 layer with a "
+                                 "dynamic scale")
+            kw = dict(scale_cols=nl.w.K, scale=nl.a_scale, scale_workspace=nl.sws,
+                      stream=stream, workspace=self.gws, geglu=self.geglu, bias=w.bias,
+                      act_cols=self.act_cols, out=self.out)
+            if w.kind == "e4m3":
+                return frt.frt_gemm_fp8_next_scale(self.q, self.a_scale, w.packed, w.w_scale, w.N,
+                                                   **kw)[0]
+            return frt.frt_gemm_bf16_next_scale(x, w.packed, w.N, w_scale=w.w_scale, **kw)[0]
         if w.kind == "e4m3":
             return frt.frt_gemm_fp8(self.q, self.a_scale, w.packed, w.w_scale, w.N, bias=w.bias,
                                     act_cols=self.act_cols, out=self.out, stream=stream,

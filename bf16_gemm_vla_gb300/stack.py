@@ -9,8 +9,11 @@ a pi0.5-style pass:
 
   encoder: 18 layers at M = 768, hidden 2048, FP8 -- QKV 2048->2560,
            O 2048->2048, merged gate/up 2048->2x16384 (tanh-GELU on the gate
-           half), down 16384->2048; every GEMM preceded by a per-tensor
-           activation quantize;
+           half), down 16384->2048; every GEMM's input quantized per tensor
+           (the first one by the activation quantize; for each later one the
+           previous GEMM takes the scale from its own output in its
+           epilogue, and the quantize is the encode pass alone; with
+           fuse_quantize=False a full quantize, amax included, each);
   decoder: 18 layers at M = 50, hidden 1024, BF16 -- QKV 1024->2560,
            O 2048->1024, gate/up 1024->2x4096, down 4096->1024.
 
@@ -36,11 +39,14 @@ M_DEC = 50
 
 class SyntheticStack:
     def __init__(self, n_layers=18, seed=1, device="cuda", enc_kind="e4m3", dec_kind="bf16",
-                 keep=(0, 17), parts=("enc", "dec")):
+                 keep=(0, 17), parts=("enc", "dec"), fuse_quantize=True):
         """parts: the chains to build ("enc", "dec" or both); a chain left out
         is empty and its weights are not drawn (the other chain's draws are
-        then not those of the full stack)."""
+        then not those of the full stack).  fuse_quantize: an FP8 layer fed
+        by a GEMM gets its input's scale from that GEMM's epilogue, so its
+        quantize is the encode pass alone."""
         self.device = torch.device(device)
+        self.fuse_quantize = fuse_quantize
         self.n_layers = n_layers
         g = torch.Generator(device=self.device)
         g.manual_seed(seed)
@@ -66,31 +72,31 @@ class SyntheticStack:
             out.append(lay)
         return out
 
-    @staticmethod
-    def _run_chain(chain, x, stream):
-        for lay in chain:
-            qkv = lay["qkv"](x, stream)
-            o = lay["o"](qkv[:, : lay["o"].w.K], stream)
-            gu = lay["gate_up"](o, stream)
-            x = lay["down"](gu[:, : lay["down"].w.K], stream)
-        return x
-
     def op_list(self):
         """Every launch of one forward in order, as (part, layer, name, op,
-        lin, call): op is "quantize" (FP8 layers only) or "gemm", lin the
-        layer's Linear, and call(stream) enqueues the launch on the buffers
-        the forward uses."""
+        lin, call): op is "quantize" (a full activation quantize), "encode"
+        (the quantize of an input whose scale the GEMM before it took),
+        "gemm", or "gemm+scale" (the GEMM also takes the next, FP8, layer's
+        input scale); lin is the layer's Linear, and call(stream) enqueues
+        the launch on the buffers the forward uses."""
         ops = []
         for part, chain in (("enc", self.enc), ("dec", self.dec)):
-            for li, lay in enumerate(chain):
-                for name in ("qkv", "o", "gate_up", "down"):
-                    lin = lay[name]
-                    x = self.inputs_of(part, li, name)
-                    if lin.w.kind == "e4m3":
-                        ops.append((part, li, name, "quantize", lin,
-                                    lambda s=None, lin=lin, x=x: lin.quantize(x, s)))
-                    ops.append((part, li, name, "gemm", lin,
-                                lambda s=None, lin=lin, x=x: lin.gemm(x, s)))
+            flat = [(li, name, lay[name]) for li, lay in enumerate(chain)
+                    for name in ("qkv", "o", "gate_up", "down")]
+            scaled = False  # this layer's input scale was taken by the previous GEMM
+            for i, (li, name, lin) in enumerate(flat):
+                x = self.inputs_of(part, li, name)
+                nl = flat[i + 1][2] if i + 1 < len(flat) else None
+                fuse = (self.fuse_quantize and nl is not None and nl.w.kind == "e4m3"
+                        and not nl.static)
+                if lin.w.kind == "e4m3":
+                    ops.append((part, li, name, "encode" if scaled else "quantize", lin,
+                                lambda s=None, lin=lin, x=x, r=scaled:
+                                lin.quantize(x, s, scale_ready=r)))
+                ops.append((part, li, name, "gemm+scale" if fuse else "gemm", lin,
+                            lambda s=None, lin=lin, x=x, nl=(nl if fuse else None):
+                            lin.gemm(x, s, next_layer=nl)))
+                scaled = fuse
         return ops
 
     def inputs_of(self, part, li, name):
@@ -108,15 +114,18 @@ class SyntheticStack:
         return lay["gate_up"].out[:, : lay["down"].w.K]
 
     def forward(self, stream=None):
-        """One eager pass (encoder chain, then decoder chain)."""
-        e = self._run_chain(self.enc, self.x_enc, stream)
-        d = self._run_chain(self.dec, self.x_dec, stream)
+        """One eager pass (encoder chain, then decoder chain); returns the last
+        layer's output of each chain (its input where the chain is empty)."""
+        for op in self.op_list():
+            op[-1](stream)
+        e = self.enc[-1]["down"].out if self.enc else self.x_enc
+        d = self.dec[-1]["down"].out if self.dec else self.x_dec
         return e, d
 
     def launches_per_forward(self):
-        """Kernels one forward launches, counted by the library (an FP8
-        layer's quantize takes one grid when its input is dense and fits on
-        chip, else two; every GEMM is one)."""
+        """Kernels one forward launches, counted by the library (a full
+        quantize takes one grid when its input is dense and fits on chip,
+        else two; an encode with a given scale and every GEMM one)."""
         n0 = frt.frt_launch_count()
         self.forward()
         torch.cuda.synchronize(self.device)

@@ -307,6 +307,56 @@ frt_status frt_gemm_bf16(const void* a, int64_t lda, const void* w_packed, const
                          size_t workspace_bytes, int* dev_status, frt_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * GEMM that also takes the next FP8 layer's activation scale from its own
+ * output.  The per-layer activation quantize is what the method spends
+ * separate launches and passes on between the GEMMs ("Real-time VLA
+ * inference on AMD hardware", "Fusing the BF16 decoder boundary", on the
+ * launch count of a replayed forward); the part of it that reads the whole
+ * tensor, the amax, is taken here in the epilogue of the GEMM that produces
+ * the tensor, so the quantize left is one encode pass over the stored output
+ * (frt_quantize_e4m3 with static_scale = scale).
+ *
+ * Computes exactly what frt_gemm_fp8 / frt_gemm_bf16 compute (same arguments,
+ * same out) and, in the same launch,
+ *   scale[0] = amax / 448 over the bf16 values out[0:M, 0:scale_cols]
+ *              (NaN ignored; 1 if amax == 0; one IEEE fp32 division),
+ * which is bit for bit the scale frt_quantize_e4m3(out[:, :scale_cols], per
+ * tensor, OCP) computes; quantizing that view with static_scale = scale then
+ * gives the same bytes as the dynamic quantize.
+ *
+ * scale_cols     : 1 <= scale_cols <= the output's columns (N, or N / 2 for
+ *                  FRT_ACT_GEGLU), a multiple of 8 (else
+ *                  FRT_ERR_UNSUPPORTED_SHAPE): the next layer reads the
+ *                  first scale_cols columns.
+ * scale          : device, receives the scale (1 float); required.
+ * scale_workspace: device memory of frt_gemm_next_scale_workspace_bytes()
+ *                  bytes, 16-byte aligned, zero-filled before its first use;
+ *                  each CTA folds its maximum into it and the last one to do
+ *                  so writes the scale and leaves it zero again.  No CTA
+ *                  waits for another.  Calls that share it must be ordered
+ *                  on one stream.
+ * workspace, dev_status, stream: as for frt_gemm_fp8.
+ * Allocates nothing; legal under stream capture.
+ * ---------------------------------------------------------------------- */
+size_t frt_gemm_next_scale_workspace_bytes(void);
+
+frt_status frt_gemm_fp8_next_scale(const uint8_t* a_q, int64_t lda, const float* a_scale,
+                                   const void* w_packed, const float* w_scale, const float* bias,
+                                   int64_t M, int64_t N, int64_t K, frt_act act, int64_t act_cols,
+                                   void* out, int64_t ldo, int64_t scale_cols, float* scale,
+                                   void* scale_workspace, size_t scale_workspace_bytes,
+                                   void* workspace, size_t workspace_bytes, int* dev_status,
+                                   frt_stream_t stream);
+
+frt_status frt_gemm_bf16_next_scale(const void* a, int64_t lda, const void* w_packed,
+                                    const float* w_scale, const float* bias, int64_t M, int64_t N,
+                                    int64_t K, frt_act act, int64_t act_cols, void* out,
+                                    int64_t ldo, int64_t scale_cols, float* scale,
+                                    void* scale_workspace, size_t scale_workspace_bytes,
+                                    void* workspace, size_t workspace_bytes, int* dev_status,
+                                    frt_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * The BF16 decoder block boundary in one kernel ("Real-time VLA inference on
  * AMD hardware", "Fusing the BF16 decoder boundary"), for each row m of an
  * [M x H] tensor:

@@ -34,7 +34,7 @@ def test_header_declares_the_binding(lib):
 def test_library_exports_every_header_symbol(lib):
     for name in header_functions():
         assert hasattr(lib, name), name
-    assert lib.frt_abi_version() == 2
+    assert lib.frt_abi_version() == 3
     assert lib.frt_launch_count() >= 0
 
 

@@ -85,8 +85,30 @@ def test_stack_graph_matches_oracle_at_first_and_last_layer():
     torch.cuda.synchronize()
     assert torch.equal(e_out, st.enc[-1]["down"].out)
     assert torch.equal(d_out, st.dec[-1]["down"].out)
-    # every FP8 layer: a quantize of one grid (dense input that fits on chip)
-    # or two, then one GEMM; every BF16 layer: one GEMM
+    # one GEMM per layer; every FP8 layer's input is quantized by one launch:
+    # the encoder's input by a full quantize (768 x 2048 dense bf16: one
+    # grid), every later one by the encode pass with the scale the GEMM
+    # before it took
     n = st.launches_per_forward()
-    assert 18 * 4 * 2 + 18 * 4 <= n <= 18 * 4 * 3 + 18 * 4
+    assert n == 18 * 4 + 18 * 4 + 18 * 4
     assert st.launches_per_forward() == n
+
+
+def test_fused_scale_stack_equals_separate_quantize_stack():
+    # the same stack with each FP8 layer's input quantized by a full quantize
+    # (amax included): every layer's bf16 output, quantized bytes and scale
+    # are equal bit for bit (the scale a GEMM takes is that of its stored
+    # output)
+    xe, xd = synth.stack_inputs(seed=1)
+    outs = []
+    for fuse in (True, False):
+        st = SyntheticStack(n_layers=18, seed=1, keep=(), fuse_quantize=fuse, parts=("enc",))
+        st.x_enc.copy_(bf16_dev(xe))
+        st.forward()
+        torch.cuda.synchronize()
+        frt.check_device_status()
+        outs.append([(lay[n].out.clone(), lay[n].q.clone(), lay[n].a_scale.clone())
+                     for lay in st.enc for n in ("qkv", "o", "gate_up", "down")])
+        del st
+    for (o1, q1, s1), (o2, q2, s2) in zip(*outs):
+        assert torch.equal(o1, o2) and torch.equal(q1, q2) and torch.equal(s1, s2)
