@@ -920,7 +920,9 @@ __global__ void __launch_bounds__(kThreads, 1)
               __stcg(dst + q * kTile + row,
                      make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]));
           }
-          __threadfence();
+          // every epilogue thread's partial stores happen before the counter
+          // increments below: the CTA barrier orders them before the
+          // signalling thread's release, which is cumulative over them
           dev::named_sync(1, 128);
           if (et == 0) {
             for (int o = 0; o < S; ++o)
@@ -1403,10 +1405,14 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int esize, bool fp8, size_t ws_a
   const bool whole_kb = (K * esize) % kKBytes == 0;
   pl.kbs = (pl.pair && whole_kb && kb >= 2) ? ((pl.bn == 128 && kb >= 8) ? 4 : 2) : 1;
   int stage_bytes = pl.kbs * (act_rows + w_rows) * kKBytes;
-  // a split's K range is a whole number of stages
+  // a split's K range: a whole number of stages (cluster splits), or as even
+  // as the split allows (splits through the workspace: a stage that runs
+  // past the range is loaded whole and multiplied only as far as the range
+  // goes, and the splits finish together)
   auto split_kb = [&](int s) {
     return static_cast<int>(ceil_div(ceil_div(kb, s), pl.kbs) * pl.kbs);
   };
+  auto split_kb_even = [&](int s) { return static_cast<int>(ceil_div(kb, s)); };
 
   int s_max = 1, g_max = 1;
   // (a pair's GeGLU tile is finished whole: its gate and up halves would
@@ -1427,7 +1433,7 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int esize, bool fp8, size_t ws_a
   Plan gpl = pl;
   bool have_g = false;
   for (int s = g_max; s >= 2 && !have_g; --s) {
-    gpl.kb_per_split = split_kb(s);
+    gpl.kb_per_split = split_kb_even(s);
     gpl.splits = static_cast<int>(ceil_div(kb, gpl.kb_per_split));
     if (gpl.splits < 2) break;
     gpl.split_global = true;
