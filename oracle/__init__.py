@@ -23,5 +23,6 @@ Modules:
   convert   -- FNUZ -> OCP re-encoding of bytes
   pack      -- the packed weight layout and its inverse
   gemm      -- fp64 GEMM on decoded values with the scale/bias/GELU epilogue
+  nvfp4     -- E2M1 codes with E4M3 block scales: quantize, decode, GEMM
 """
-from . import e4m3, bf16, quantize, convert, pack, gemm  # noqa: F401
+from . import e4m3, bf16, quantize, convert, pack, gemm, nvfp4  # noqa: F401
