@@ -789,9 +789,71 @@ def run_components(args, device, sampler, peaks):
                                                                        secs)}
     del st
     torch.cuda.empty_cache()
+    out["nvfp4_encoder_ffn_m768"] = nvfp4_ffn(device, sampler, peaks)
     if not args.no_sweep:
         out["sweep_k4096_n4096"] = run_sweep(device, sampler, peaks)
     return out
+
+
+FP4_OVER_BF16 = 6.0  # nominal dense ratio, 13.5 / 2.25 PFLOP/s
+
+
+def nvfp4_ffn(device, sampler, peaks):
+    """The encoder FFN on NVFP4 operands at M = 768: the merged gate/up
+    2048 -> 2 x 16384 (GELU on the gate half) and down 16384 -> 2048, each
+    GEMM back to back over rotating weight copies (> 4x L2), and the NVFP4
+    activation quantize (amax + encode) of each input.  The fraction is of
+    the dense FP4 peak taken as the measured BF16 burst x 6 (nominal ratio;
+    no FP4 measurement)."""
+    from bf16_gemm_vla_gb300 import frt, layers
+
+    fp4_peak = peaks["bf16_tflops"] * FP4_OVER_BF16
+    g = torch.Generator(device=device)
+    g.manual_seed(12)
+    rows = []
+    for K, N, act in ((2048, 2 * 16384, 16384), (16384, 2048, 0)):
+        w = torch.randn((K, N), generator=g, device=device) * 0.02
+        b = torch.randn((N,), generator=g, device=device) * 0.1
+        pw = layers.prepare_nvfp4(w, b)
+        del w
+        wbytes = pw.packed.numel() + pw.sf.numel()
+        copies = min(64, max(4, -(-4 * l2_bytes() // wbytes)))
+        ws = [(pw.packed, pw.sf)] + [(pw.packed.clone(), pw.sf.clone()) for _ in range(copies - 1)]
+        x = torch.randn((M_ENC, K), generator=g, device=device).to(torch.bfloat16)
+        qa, sfa, ga = frt.frt_quantize_nvfp4(x)
+        out = torch.empty((M_ENC, N), dtype=torch.bfloat16, device=device)
+        torch.cuda.synchronize()
+
+        def run_gemm():
+            for pk, sf in ws:
+                frt.frt_gemm_nvfp4(qa, sfa, ga, pk, sf, pw.g, N, bias=b, act_cols=act, out=out)
+
+        gr = capture(run_gemm)
+        gr.replay()
+        t0 = time.time()
+        per = device_time(lambda i: gr.replay(), 5) / (5 * copies)
+        sampler.window(t0, time.time())
+        nws = frt.nvfp4_workspace(device)
+
+        def run_quant():
+            for _ in range(16):
+                frt.frt_quantize_nvfp4(x, q=qa, sf=sfa, scale=ga, workspace=nws)
+
+        gq = capture(run_quant)
+        gq.replay()
+        qper = device_time(lambda i: gq.replay(), 5) / (5 * 16)
+        frt.check_device_status()
+        tf = 2.0 * M_ENC * N * K / per / 1e12
+        rows.append({"K": K, "N": N, "act_cols": act, "us": per * 1e6, "tflops": tf,
+                     "frac_of_fp4_peak": tf / fp4_peak, "weight_bytes": wbytes,
+                     "quantize_us": qper * 1e6, "copies": copies})
+        del ws, gr, gq, pw
+        torch.cuda.empty_cache()
+    return {"layers": rows, "fp4_peak": fp4_peak,
+            "peak_source": "measured bf16 burst x %.0f (nominal FP4/BF16 dense ratio)"
+                           % FP4_OVER_BF16,
+            "kernel": "gemm_nvfp4_kernel (128x128 tiles, tcgen05 kind::mxf4nvf4 with E4M3 "
+                      "block scales per 16)"}
 
 
 def run_sweep(device, sampler, peaks):

@@ -54,6 +54,12 @@ SIGNATURES = {
     "frt_gemm_bf16_next_scale": (_c_int, [_c_p, _c_i64, _c_p, _c_p, _c_p, _c_i64, _c_i64, _c_i64,
                                           _c_int, _c_i64, _c_p, _c_i64, _c_i64, _c_p, _c_p, _c_sz,
                                           _c_p, _c_sz, _c_p, _c_p]),
+    "frt_nvfp4_scale_bytes": (_c_sz, [_c_i64, _c_i64]),
+    "frt_quantize_nvfp4_workspace_bytes": (_c_sz, []),
+    "frt_quantize_nvfp4": (_c_int, [_c_p, _c_int, _c_i64, _c_i64, _c_i64, _c_int, _c_p, _c_p,
+                                    _c_p, _c_sz, _c_p, _c_p, _c_sz, _c_p]),
+    "frt_gemm_nvfp4": (_c_int, [_c_p, _c_i64, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_i64,
+                                _c_i64, _c_i64, _c_int, _c_i64, _c_p, _c_i64, _c_p, _c_p]),
     "frt_gate_residual_ada_norm_bf16": (_c_int, [_c_p, _c_p, _c_p, _c_p, _c_i64, _c_i64,
                                                  ctypes.c_float, _c_p, _c_p, _c_p]),
     "frt_gemm_fp8": (_c_int, [_c_p, _c_i64, _c_p, _c_p, _c_p, _c_p, _c_i64, _c_i64, _c_i64,

@@ -18,7 +18,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB_PATH = os.path.join(HERE, "libfrt.so")
 
-SOURCES = ["frt_common.cu", "frt_casts.cu", "frt_pack.cu", "frt_gemm.cu", "frt_norm.cu"]
+SOURCES = ["frt_common.cu", "frt_casts.cu", "frt_pack.cu", "frt_gemm.cu", "frt_norm.cu",
+           "frt_nvfp4.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
                 "-I" + INCLUDE, "-I" + CSRC]

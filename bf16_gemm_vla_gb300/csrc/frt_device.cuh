@@ -213,6 +213,49 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// Shared-memory matrix descriptor of a tile with no swizzle: core matrices
+// of 8 rows x 16 bytes (128 contiguous bytes); lbo / sbo are the byte
+// distances between core matrices along K / along the rows.
+__device__ __forceinline__ uint64_t smem_desc_noswz(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+  d |= static_cast<uint64_t>(1) << 46;  // descriptor version; layout 0 = no swizzle
+  return d;
+}
+
+// Copies 32 rows of 128 bits from shared memory (descriptor sdesc) into TMEM
+// columns [taddr, taddr + 4) of lanes 0-31, the same rows into each of the
+// four 32-lane quarters (.warpx4).  Ordered with the issuing thread's later
+// tcgen05.mma.
+__device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
+               : "memory");
+}
+
+// Block-scaled E2M1 x E2M1 MMA (kind::mxf4nvf4, one E4M3 scale per 16
+// elements of K for each row of A and each column of B, read from TMEM at
+// tsfa / tsfb), fp32 accumulator in TMEM.
+__device__ __forceinline__ void mma_nvfp4(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
+                                          uint32_t idesc, uint32_t tsfa, uint32_t tsfb,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, "
+      "[%5], [%6], p;\n\t}" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(tsfa), "r"(tsfb)
+      : "memory");
+}
+
+// Instruction descriptor of the block-scaled kinds: E2M1 operands (format 1
+// of kind::mxf4nvf4), both K-major, scale factors E4M3 (scale format 0),
+// scale-factor ids 0, shape M x N; the accumulator is fp32.
+__host__ __device__ constexpr uint32_t instr_desc_nvfp4(int m, int n) {
+  return (1u << 7) | (1u << 10) | (static_cast<uint32_t>(n >> 3) << 17) |
+         (static_cast<uint32_t>(m >> 4) << 24);
+}
+
 // ---------------------------------------------------------------- clusters
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {

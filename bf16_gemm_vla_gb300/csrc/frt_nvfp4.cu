@@ -1,0 +1,612 @@
+// NVFP4 (block-scaled 4-bit floats): quantize and GEMM.
+//
+// The FlashRT article names an NVFP4 path beside FP8 for the pi0.5 encoder
+// FFN (section 7.2 of its table of contents, "NVFP4 path"; the use_fp4 /
+// fp4_layers switches of its load_model listing) and gives no formula.  The
+// format is read as E2M1 elements with one E4M3 scale per 16 consecutive
+// elements along the reduction dimension K and one fp32 scale g per tensor
+// (frt.h states the steps).
+//
+//   * Quantize: pass 1 folds the CTAs' maxima |x| into a workspace word;
+//     pass 2 gives each thread one 16-element block: block maximum, E4M3
+//     block scale, E2M1 codes (two per byte), and writes the block scale in
+//     the GEMM's tiled layout.  The last CTA of pass 2 clears the workspace.
+//   * GEMM: 128 x 128 output tiles, one CTA each, persistent.  A pipeline
+//     stage holds one 256-element k-block of both operands (codes, 128 bytes
+//     per row, 128-byte swizzle) and their four + four 512-byte scale atoms.
+//     The MMA thread copies each atom into TMEM (tcgen05.cp) and issues the
+//     block-scaled MMA (kind::mxf4nvf4, K = 64, four per k-block); the
+//     epilogue multiplies by g_a g_w, adds the bias, applies the GELU and
+//     stores bf16 by TMA.
+//
+// Scale layout ("tiled"), for a tensor of V vectors (rows of A, output
+// channels of W) blocked along K: the scale of vector v, block j sits at
+//   ((v / 128) * (K / 64) + j / 4) * 512 + 16 * (v % 32) + 4 * ((v % 128) / 32) + j % 4,
+// so one 512-byte atom holds 128 vectors x 4 blocks (64 elements of K) as
+// 32 lines of 16 bytes; line i carries vectors i, i + 32, i + 64, i + 96.
+// tcgen05.cp .32x128b.warpx4 puts line i into TMEM lane i of every 32-lane
+// quarter, 4 columns wide, which is where the MMA reads the scales of the
+// 128 rows of one K = 64 step.
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "frt_device.cuh"
+#include "frt_e4m3.cuh"
+#include "frt_epilogue.cuh"
+#include "frt_host.h"
+#include "frt_tma_host.h"
+
+namespace frt {
+namespace {
+
+constexpr int kBlk = 16;  // elements per block scale
+constexpr float kNvMaxProduct = 6.0f * 448.0f;  // E2M1 max x E4M3 max
+
+__host__ __device__ inline int64_t sf_offset(int64_t v, int64_t j, int64_t kc_total) {
+  return ((v / 128) * kc_total + j / 4) * 512 + 16 * (v % 32) + 4 * ((v % 128) / 32) + (j % 4);
+}
+
+// ------------------------------------------------------------------ element codes
+
+// E2M1 code of an fp32 value, round to nearest with ties to the even code.
+// The magnitudes are 0, 0.5, 1, 1.5, 2, 3, 4, 6 (codes 0..7); between two
+// neighbours the midpoint goes to the one with mantissa bit 0: 0.25 -> 0,
+// 0.75 -> 1, 1.25 -> 1, 1.75 -> 2, 2.5 -> 2, 3.5 -> 4, 5 -> 4; from 6 up
+// (infinity included) the code saturates at 6.  The sign bit is kept, a
+// value that rounds to zero included; NaN gives +0.
+__device__ __forceinline__ uint32_t e2m1_code(float y) {
+  if (!(y == y)) return 0u;
+  const uint32_t sign = (__float_as_uint(y) >> 28) & 8u;
+  const float a = fabsf(y);
+  const uint32_t c = (a > 0.25f) + (a >= 0.75f) + (a > 1.25f) + (a >= 1.75f) + (a > 2.5f) +
+                     (a >= 3.5f) + (a > 5.0f);
+  return sign | c;
+}
+
+// Value of a non-negative OCP E4M3 byte (no NaN: the block scales saturate).
+__device__ __forceinline__ float e4m3_value_pos(uint32_t b) {
+  const uint32_t e = (b >> 3) & 15u, m = b & 7u;
+  return e == 0 ? static_cast<float>(m) * 0x1p-9f
+                : __uint_as_float(((e + 120u) << 23) | (m << 20));  // (1 + m/8) 2^(e-7)
+}
+
+template <typename T>
+__device__ __forceinline__ float nv_to_f32(T v);
+template <>
+__device__ __forceinline__ float nv_to_f32<float>(float v) { return v; }
+template <>
+__device__ __forceinline__ float nv_to_f32<__nv_bfloat16>(__nv_bfloat16 v) {
+  return __bfloat162float(v);
+}
+
+// ------------------------------------------------------------------ quantize
+
+constexpr int kNvQThreads = 256;
+
+template <typename T>
+__global__ void __launch_bounds__(kNvQThreads) nvfp4_amax_kernel(const T* __restrict__ x,
+                                                                  int64_t rows, int64_t cols,
+                                                                  int64_t ldx, unsigned* ws) {
+  __shared__ float red[kNvQThreads / 32];
+  dev::grid_dependency_wait();  // x may come from the previous grid
+  float m = 0.0f;
+  for (int64_t r = blockIdx.y; r < rows; r += gridDim.y)
+    for (int64_t c = static_cast<int64_t>(blockIdx.x) * kNvQThreads + threadIdx.x; c < cols;
+         c += static_cast<int64_t>(gridDim.x) * kNvQThreads)
+      m = fmaxf(m, fabsf(nv_to_f32<T>(x[r * ldx + c])));  // NaN is ignored by fmaxf
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < kNvQThreads / 32; ++w) m = fmaxf(m, red[w]);
+    if (m > 0.0f) atomicMax(ws, __float_as_uint(m));  // m >= 0: bits order as values
+  }
+  dev::grid_launch_dependents();
+}
+
+// One thread per (vector v, block j).  kAlongRows: x is [K x V] (blocks run
+// down the columns, e.g. a weight W[K x N]); else x is [V x K].  Codes are
+// written in x's orientation, two per byte along K (element 2i in the low
+// nibble): [V x K/2] or [K/2 x V]; block scales in the tiled layout, the
+// vectors past V (up to the next multiple of 128) with scale 0.
+template <typename T, bool kAlongRows>
+__global__ void __launch_bounds__(kNvQThreads) nvfp4_encode_kernel(
+    const T* __restrict__ x, int64_t V, int64_t Kd, int64_t ldx, const float* static_scale,
+    unsigned* ws, uint8_t* __restrict__ q, uint8_t* __restrict__ sf, float* scale_out) {
+  __shared__ float g_sh;
+  dev::grid_dependency_wait();  // x, the amax word and a static scale come from earlier grids
+  if (threadIdx.x == 0) {
+    float g;
+    if (static_scale) {
+      g = __ldcg(static_scale);
+    } else {
+      const float amax = __uint_as_float(__ldcg(ws));
+      g = amax == 0.0f ? 1.0f : __fdiv_rn(amax, kNvMaxProduct);
+    }
+    g_sh = g;
+    if (blockIdx.x == 0 && scale_out) *scale_out = g;
+  }
+  __syncthreads();
+  const float g = g_sh;
+  const float d = __fmul_rn(6.0f, g);
+  const int64_t nb = Kd / kBlk;             // blocks per vector
+  const int64_t vpad = (V + 127) / 128 * 128;
+  const int64_t kc_total = Kd / 64;
+  const int64_t total = vpad * nb;
+  for (int64_t t = static_cast<int64_t>(blockIdx.x) * kNvQThreads + threadIdx.x; t < total;
+       t += static_cast<int64_t>(gridDim.x) * kNvQThreads) {
+    int64_t v, j;
+    if constexpr (kAlongRows) {  // consecutive threads: consecutive columns (coalesced)
+      v = t % vpad;
+      j = t / vpad;
+    } else {  // consecutive threads: consecutive blocks of a row
+      v = t / nb;
+      j = t % nb;
+    }
+    uint32_t sbyte = 0u;
+    if (v < V) {
+      float f[kBlk];
+      if constexpr (kAlongRows) {
+#pragma unroll
+        for (int i = 0; i < kBlk; ++i) f[i] = nv_to_f32<T>(x[(j * kBlk + i) * ldx + v]);
+      } else if constexpr (sizeof(T) == 2) {
+        const uint4* src = reinterpret_cast<const uint4*>(x + v * ldx + j * kBlk);
+        const uint4 w0 = src[0], w1 = src[1];
+        const uint32_t ws8[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          f[2 * k] = __uint_as_float(ws8[k] << 16);
+          f[2 * k + 1] = __uint_as_float(ws8[k] & 0xFFFF0000u);
+        }
+      } else {
+        const float4* src = reinterpret_cast<const float4*>(x + v * ldx + j * kBlk);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float4 a = src[k];
+          f[4 * k] = a.x; f[4 * k + 1] = a.y; f[4 * k + 2] = a.z; f[4 * k + 3] = a.w;
+        }
+      }
+      float b = 0.0f;
+#pragma unroll
+      for (int i = 0; i < kBlk; ++i) b = fmaxf(b, fabsf(f[i]));
+      sbyte = encode_e4m3<false>(__fdiv_rn(b, d));  // b >= 0, d > 0: a non-negative byte
+      const float e = __fmul_rn(e4m3_value_pos(sbyte), g);
+      uint32_t c[kBlk];
+#pragma unroll
+      for (int i = 0; i < kBlk; ++i) c[i] = e > 0.0f ? e2m1_code(__fdiv_rn(f[i], e)) : 0u;
+      if constexpr (kAlongRows) {
+        // [K/2 x V]: byte (8 j + p, v) holds elements 16 j + 2 p (low) and + 1
+#pragma unroll
+        for (int p2 = 0; p2 < kBlk / 2; ++p2)
+          q[(j * (kBlk / 2) + p2) * V + v] = static_cast<uint8_t>(c[2 * p2] | (c[2 * p2 + 1] << 4));
+      } else {
+        uint32_t lo = 0u, hi = 0u;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          lo |= c[i] << (4 * i);
+          hi |= c[8 + i] << (4 * i);
+        }
+        *reinterpret_cast<uint2*>(q + v * (Kd / 2) + j * (kBlk / 2)) = make_uint2(lo, hi);
+      }
+    }
+    sf[sf_offset(v, j, kc_total)] = static_cast<uint8_t>(sbyte);
+  }
+  // the amax word is read by every CTA before it counts itself done here; the
+  // last one clears it (and the count) for the next call
+  if (!static_scale) {
+    __syncthreads();
+    if (threadIdx.x == 0 && atomicAdd(ws + 1, 1u) == gridDim.x - 1) {
+      ws[0] = 0u;
+      ws[1] = 0u;
+    }
+  }
+  dev::grid_launch_dependents();
+}
+
+// ------------------------------------------------------------------ GEMM
+
+constexpr int kNvThreads = 192;  // copy warp, MMA warp, 4 epilogue warps
+constexpr int kNvStages = 4;
+constexpr int kNvTile = 128;
+constexpr int kNvOpBytes = kNvTile * 128;  // codes of one operand per k-block (256 elements)
+constexpr int kNvSfBytes = 4 * 512;        // 4 scale atoms per operand per k-block
+constexpr int kNvStageBytes = 2 * kNvOpBytes + 2 * kNvSfBytes;
+constexpr int kNvOutOff = kNvStages * kNvStageBytes;
+constexpr int kNvBiasOff = kNvOutOff + 4 * 2 * kWarpOutBytes;
+constexpr int kNvBarOff = kNvBiasOff + 2 * kNvTile * 4;
+constexpr int kNvSmem = 1024 + kNvBarOff + 256;
+constexpr uint32_t kNvTmemCols = 512;      // 2 accumulators of 128 columns, then scales
+constexpr uint32_t kNvSfCol0 = 2 * kNvTile;  // per stage: 16 columns A scales, 16 B scales
+
+struct NvGemmArgs {
+  const uint8_t* a_sf;
+  const uint8_t* w_packed;
+  const uint8_t* w_sf;
+  const float* a_scale;  // g_a (1 float) or null (= 1)
+  const float* w_scale;  // g_w (1 float) or null (= 1)
+  const float* bias;     // N floats or null
+  int M, N, act_cols;
+  int kb_total;  // 256-element k-blocks
+  int kc_total;  // 64-element scale chunks (K / 64)
+  int tiles_m, num_tiles;
+  int* dev_status;
+};
+
+__global__ void __launch_bounds__(kNvThreads, 1)
+    gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                      const __grid_constant__ CUtensorMap tmap_out, const NvGemmArgs p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = smem_raw + ((1024u - (dev::smem_u32(smem_raw) & 1023u)) & 1023u);
+  const uint32_t sbase = dev::smem_u32(base);
+  float* bias_s = reinterpret_cast<float*>(base + kNvBiasOff);  // [2 tiles][128 channels]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base + kNvBarOff);
+  const uint32_t full0 = dev::smem_u32(bars);
+  const uint32_t empty0 = full0 + 8 * kNvStages;
+  const uint32_t tfull0 = empty0 + 8 * kNvStages;
+  const uint32_t tempty0 = tfull0 + 16;
+  const uint32_t scale_bar = tempty0 + 16;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kNvStages + 5);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float* gscale_s = reinterpret_cast<float*>(tmem_slot + 2);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kNvStages; ++s) {
+      dev::mbar_init(full0 + 8 * s, 1);
+      dev::mbar_init(empty0 + 8 * s, 1);
+    }
+    dev::mbar_init(tfull0, 1);
+    dev::mbar_init(tfull0 + 8, 1);
+    dev::mbar_init(tempty0, 4);
+    dev::mbar_init(tempty0 + 8, 4);
+    dev::mbar_init(scale_bar, 1);
+    *abort_flag = 0;
+    dev::fence_mbar_init();
+    dev::prefetch_tmap(&tmap_a);
+    dev::prefetch_tmap(&tmap_out);
+  }
+  if (warp == 1) dev::tmem_alloc(dev::smem_u32(tmem_slot), kNvTmemCols);
+  dev::tc_fence_before();
+  __syncthreads();
+  dev::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  dev::grid_launch_dependents();
+
+  const int first = static_cast<int>(blockIdx.x);
+  const int step = static_cast<int>(gridDim.x);
+  const int my_tiles = first < p.num_tiles ? (p.num_tiles - first + step - 1) / step : 0;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ copies
+      const uint64_t pol_w = dev::policy_evict_normal();
+      const uint64_t pol_a = dev::policy_evict_last();
+      // the activations, their scales and g_a come from the previous grid
+      dev::grid_dependency_wait();
+      *gscale_s = __fmul_rn(p.a_scale ? __ldcg(p.a_scale) : 1.0f,
+                            p.w_scale ? __ldcg(p.w_scale) : 1.0f);
+      dev::mbar_arrive(scale_bar);
+      int s = 0, issued = 0;
+      uint32_t ph = 0;
+      bool stop = false;
+      for (int it = 0; it < my_tiles && !stop; ++it) {
+        const int t = first + it * step;
+        const int tm = t % p.tiles_m, tn = t / p.tiles_m;
+        for (int kb = 0; kb < p.kb_total; ++kb) {
+          if (!dev::mbar_wait(empty0 + 8 * s, (ph & 1) ^ 1, abort_flag, p.dev_status,
+                              dev::kTimeoutProducer)) {
+            stop = true;
+            break;
+          }
+          const uint32_t st = sbase + s * kNvStageBytes;
+          const uint32_t fb = full0 + 8 * s;
+          dev::mbar_arrive_expect_tx(fb, kNvStageBytes);
+          dev::tma_load_2d(st, &tmap_a, kb * 128, tm * kNvTile, fb, pol_a);
+          dev::bulk_load(st + kNvOpBytes,
+                         p.w_packed + (static_cast<size_t>(tn) * p.kb_total + kb) * kNvOpBytes,
+                         kNvOpBytes, fb, pol_w);
+          dev::bulk_load(st + 2 * kNvOpBytes,
+                         p.a_sf + (static_cast<size_t>(tm) * p.kc_total + 4 * kb) * 512,
+                         kNvSfBytes, fb, pol_a);
+          dev::bulk_load(st + 2 * kNvOpBytes + kNvSfBytes,
+                         p.w_sf + (static_cast<size_t>(tn) * p.kc_total + 4 * kb) * 512,
+                         kNvSfBytes, fb, pol_w);
+          ++issued;
+          if (++s == kNvStages) {
+            s = 0;
+            ++ph;
+          }
+        }
+      }
+      // no copies in flight when the CTA leaves (bounded, even after an abort)
+      for (int g = issued - kNvStages < 0 ? 0 : issued - kNvStages; g < issued; ++g)
+        dev::mbar_wait(full0 + 8 * (g % kNvStages), (g / kNvStages) & 1, nullptr, p.dev_status,
+                       dev::kTimeoutProducer);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ scales + MMA
+      constexpr uint32_t idesc = dev::instr_desc_nvfp4(kNvTile, kNvTile);
+      int s = 0;
+      uint32_t ph = 0;
+      bool stop = false;
+      for (int it = 0; it < my_tiles && !stop; ++it) {
+        const int b = it & 1;
+        const uint32_t u = static_cast<uint32_t>(it >> 1);
+        if (!dev::mbar_wait(tempty0 + 8 * b, (u & 1) ^ 1, abort_flag, p.dev_status,
+                            dev::kTimeoutMma))
+          break;
+        dev::tc_fence_after();
+        const uint32_t d = tmem + static_cast<uint32_t>(b * kNvTile);
+        for (int kb = 0; kb < p.kb_total; ++kb) {
+          if (!dev::mbar_wait(full0 + 8 * s, ph & 1, abort_flag, p.dev_status, dev::kTimeoutMma)) {
+            stop = true;
+            break;
+          }
+          dev::tc_fence_after();
+          const uint32_t st = sbase + s * kNvStageBytes;
+          const uint64_t ad = dev::smem_desc_sw128(st);
+          const uint64_t bd = dev::smem_desc_sw128(st + kNvOpBytes);
+          const uint32_t sfa = tmem + kNvSfCol0 + 32u * s;  // 16 columns of A scales,
+          const uint32_t sfb = sfa + 16u;                    // then 16 of B scales
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            dev::tmem_cp_32x128b_x4(sfa + 4u * k,
+                                    dev::smem_desc_noswz(st + 2 * kNvOpBytes + 512 * k, 128, 128));
+            dev::tmem_cp_32x128b_x4(
+                sfb + 4u * k,
+                dev::smem_desc_noswz(st + 2 * kNvOpBytes + kNvSfBytes + 512 * k, 128, 128));
+            dev::mma_nvfp4(d, ad + 2 * k, bd + 2 * k, idesc, sfa + 4u * k, sfb + 4u * k,
+                           (kb | k) != 0);
+          }
+          dev::mma_commit(empty0 + 8 * s);
+          if (++s == kNvStages) {
+            s = 0;
+            ++ph;
+          }
+        }
+        dev::mma_commit(tfull0 + 8 * b);
+      }
+    }
+  } else {
+    // -------------------------------------------------------------- epilogue
+    const int et = threadIdx.x - 64;
+    const int ew = warp & 3;  // TMEM lane quarter
+    const uint32_t lane_off = static_cast<uint32_t>(ew * 32) << 16;
+    uint8_t* wbuf = base + kNvOutOff + (warp - 2) * 2 * kWarpOutBytes;
+    const uint32_t wbuf_s = sbase + kNvOutOff + (warp - 2) * 2 * kWarpOutBytes;
+    int wb = 0;
+    bool ok = dev::mbar_wait(scale_bar, 0, abort_flag, p.dev_status, dev::kTimeoutEpilogue);
+    const float gs = *gscale_s;
+    for (int it = 0; it < my_tiles && ok; ++it) {
+      const int t = first + it * step;
+      const int tm = t % p.tiles_m, tn = t / p.tiles_m;
+      const int b = it & 1;
+      const uint32_t u = static_cast<uint32_t>(it >> 1);
+      float* bs = bias_s + (it & 1) * kNvTile;
+      {
+        const int n = tn * kNvTile + et;
+        bs[et] = (p.bias && n < p.N) ? __ldg(p.bias + n) : 0.0f;
+      }
+      dev::named_sync(1, 128);
+      ok = dev::mbar_wait(tfull0 + 8 * b, u & 1, abort_flag, p.dev_status, dev::kTimeoutEpilogue);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      dev::tc_fence_after();
+      const uint32_t tacc = tmem + lane_off + static_cast<uint32_t>(b * kNvTile);
+#pragma unroll 1
+      for (int c = 0; c < kNvTile; c += 32) {
+        float v[32];
+        dev::tmem_ld32(tacc + c, v);
+        if (c + 32 == kNvTile) {  // accumulator read out: back to the MMA thread
+          dev::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) dev::mbar_arrive(tempty0 + 8 * b);
+        }
+        const int n0 = tn * kNvTile + c;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = lin(v[j], gs, bs[c + j]);
+        if (n0 + 32 <= p.act_cols) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = gelu_tanh(v[j]);
+        } else if (n0 < p.act_cols) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const float gv = gelu_tanh(v[j]);
+            v[j] = n0 + j < p.act_cols ? gv : v[j];
+          }
+        }
+        warp_store<false, 32>(v, wbuf + wb * kWarpOutBytes, wbuf_s + wb * kWarpOutBytes,
+                              &tmap_out, n0, tm * kNvTile + ew * 32, lane);
+        wb ^= 1;
+      }
+    }
+    if (lane == 0) dev::bulk_wait_all();  // stores complete before the grid ends
+  }
+  dev::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    dev::tc_fence_after();
+    dev::tmem_dealloc(tmem, kNvTmemCols);
+  }
+}
+
+cudaError_t prepare_nvfp4_gemm() {
+  static std::mutex mu;
+  static bool set[64] = {false};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!set[dev]) {
+    const cudaError_t e = cudaFuncSetAttribute(
+        gemm_nvfp4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kNvSmem);
+    if (e != cudaSuccess) return e;
+    set[dev] = true;
+  }
+  return cudaSuccess;
+}
+
+template <typename T>
+frt_status quantize_nvfp4_typed(const T* x, int64_t rows, int64_t cols, int64_t ldx,
+                                bool along_rows, const float* static_scale, uint8_t* q,
+                                uint8_t* sf, float* scale, unsigned* ws, cudaStream_t st) {
+  const int sms = sm_count() > 0 ? sm_count() : 148;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(kNvQThreads);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaSuccess;
+  int launches = 1;
+  if (!static_scale) {
+    const int gx = static_cast<int>(std::min<int64_t>(ceil_div(cols, kNvQThreads), 64));
+    const int gy = static_cast<int>(std::min<int64_t>(rows, std::max<int64_t>(1, 4 * sms / gx)));
+    cfg.gridDim = dim3(gx, gy);
+    e = cudaLaunchKernelEx(&cfg, nvfp4_amax_kernel<T>, x, rows, cols, ldx, ws);
+    ++launches;
+  }
+  const int64_t V = along_rows ? cols : rows;
+  const int64_t Kd = along_rows ? rows : cols;
+  const int64_t total = ceil_div(V, 128) * 128 * (Kd / kBlk);
+  cfg.gridDim = dim3(static_cast<unsigned>(
+      std::max<int64_t>(1, std::min<int64_t>(ceil_div(total, kNvQThreads), 8 * sms))));
+  if (e == cudaSuccess)
+    e = along_rows ? cudaLaunchKernelEx(&cfg, nvfp4_encode_kernel<T, true>, x, V, Kd, ldx,
+                                        static_scale, ws, q, sf, scale)
+                   : cudaLaunchKernelEx(&cfg, nvfp4_encode_kernel<T, false>, x, V, Kd, ldx,
+                                        static_scale, ws, q, sf, scale);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return FRT_ERR_CUDA;
+  }
+  note_launches(launches);
+  return launch_status();
+}
+
+}  // namespace
+}  // namespace frt
+
+extern "C" size_t frt_nvfp4_scale_bytes(int64_t vectors, int64_t K) {
+  if (vectors < 1 || K < 64 || K % 64 != 0) return 0;
+  return static_cast<size_t>(frt::ceil_div(vectors, 128) * 128 * (K / 16));
+}
+
+extern "C" size_t frt_quantize_nvfp4_workspace_bytes(void) { return 16; }
+
+extern "C" frt_status frt_quantize_nvfp4(const void* x, frt_dtype x_dtype, int64_t rows,
+                                         int64_t cols, int64_t ldx, int blocks_along_rows,
+                                         const float* static_scale, uint8_t* q, uint8_t* sf,
+                                         size_t sf_bytes, float* scale, void* workspace,
+                                         size_t workspace_bytes, frt_stream_t stream) {
+  if (!x || !q || !sf) return FRT_ERR_INVALID_ARG;
+  if (x_dtype != FRT_BF16 && x_dtype != FRT_F32) return FRT_ERR_INVALID_ARG;
+  if (rows < 1 || cols < 1 || ldx < cols) return FRT_ERR_INVALID_ARG;
+  const int64_t V = blocks_along_rows ? cols : rows;
+  const int64_t Kd = blocks_along_rows ? rows : cols;
+  if (Kd % 64 != 0) return FRT_ERR_UNSUPPORTED_SHAPE;
+  if (sf_bytes < frt_nvfp4_scale_bytes(V, Kd)) return FRT_ERR_WORKSPACE_TOO_SMALL;
+  if (!static_scale && (!workspace || workspace_bytes < 16)) return FRT_ERR_WORKSPACE_TOO_SMALL;
+  const int esz = x_dtype == FRT_BF16 ? 2 : 4;
+  if (!frt::aligned(x, 16) || (ldx * esz) % 16 != 0 || !frt::aligned(q, 16) ||
+      (workspace && !frt::aligned(workspace, 16)) || (scale && !frt::aligned(scale, 4)) ||
+      (static_scale && !frt::aligned(static_scale, 4)))
+    return FRT_ERR_MISALIGNED;
+  unsigned* ws = static_cast<unsigned*>(workspace);
+  const cudaStream_t st = frt::as_cuda(stream);
+  if (x_dtype == FRT_BF16)
+    return frt::quantize_nvfp4_typed(static_cast<const __nv_bfloat16*>(x), rows, cols, ldx,
+                                     blocks_along_rows != 0, static_scale, q, sf, scale, ws, st);
+  return frt::quantize_nvfp4_typed(static_cast<const float*>(x), rows, cols, ldx,
+                                   blocks_along_rows != 0, static_scale, q, sf, scale, ws, st);
+}
+
+extern "C" frt_status frt_gemm_nvfp4(const uint8_t* a_q, int64_t lda, const uint8_t* a_sf,
+                                     const float* a_scale, const void* w_packed,
+                                     const uint8_t* w_sf, const float* w_scale, const float* bias,
+                                     int64_t M, int64_t N, int64_t K, frt_act act,
+                                     int64_t act_cols, void* out, int64_t ldo, int* dev_status,
+                                     frt_stream_t stream) {
+  using namespace frt;
+  if (!a_q || !a_sf || !w_packed || !w_sf || !out) return FRT_ERR_INVALID_ARG;
+  if (act != FRT_ACT_NONE && act != FRT_ACT_GELU_TANH) return FRT_ERR_INVALID_ARG;
+  if (M < 1 || N < 1 || K < 1 || lda < K / 2 || ldo < N) return FRT_ERR_INVALID_ARG;
+  if (act == FRT_ACT_GELU_TANH && (act_cols < 0 || act_cols > N)) return FRT_ERR_INVALID_ARG;
+  if (K % 256 != 0 || N % 16 != 0) return FRT_ERR_UNSUPPORTED_SHAPE;
+  if (M > (1LL << 31) - 1 || N > (1LL << 31) - 1 || K > (1LL << 31) - 1 ||
+      ldo > (1LL << 31) - 1)
+    return FRT_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned(a_q, 16) || lda % 16 != 0 || !aligned(a_sf, 16) || !aligned(w_packed, 16) ||
+      !aligned(w_sf, 16) || !aligned(out, 16) || ldo % 8 != 0 ||
+      (a_scale && !aligned(a_scale, 4)) || (w_scale && !aligned(w_scale, 4)) ||
+      (bias && !aligned(bias, 4)) || (dev_status && !aligned(dev_status, 4)))
+    return FRT_ERR_MISALIGNED;
+  auto encode = tensor_map_encoder();
+  if (!encode) return FRT_ERR_CUDA;
+  CUtensorMap ta, to;
+  {
+    // the codes as bytes [M x K/2], one box = 128 rows x 128 bytes (256
+    // elements), 128-byte swizzle, zero fill past M
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K / 2), static_cast<cuuint64_t>(M)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(lda)};
+    const cuuint32_t box[2] = {128u, 128u};
+    const cuuint32_t estr[2] = {1, 1};
+    if (encode(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(a_q), dims, strides,
+               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return FRT_ERR_CUDA;
+  }
+  {
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(M)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ldo * 2)};
+    const cuuint32_t box[2] = {32u, 32u};
+    const cuuint32_t estr[2] = {1, 1};
+    if (encode(&to, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, out, dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+               CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return FRT_ERR_CUDA;
+  }
+  NvGemmArgs ga;
+  ga.a_sf = a_sf;
+  ga.w_packed = static_cast<const uint8_t*>(w_packed);
+  ga.w_sf = w_sf;
+  ga.a_scale = a_scale;
+  ga.w_scale = w_scale;
+  ga.bias = bias;
+  ga.M = static_cast<int>(M);
+  ga.N = static_cast<int>(N);
+  ga.act_cols = act == FRT_ACT_GELU_TANH ? static_cast<int>(act_cols) : 0;
+  ga.kb_total = static_cast<int>(K / 256);
+  ga.kc_total = static_cast<int>(K / 64);
+  ga.tiles_m = static_cast<int>(ceil_div(M, kNvTile));
+  ga.num_tiles = ga.tiles_m * static_cast<int>(ceil_div(N, kNvTile));
+  ga.dev_status = dev_status;
+  cudaError_t e = prepare_nvfp4_gemm();
+  if (e != cudaSuccess) return FRT_ERR_CUDA;
+  const int sms = sm_count() > 0 ? sm_count() : 148;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(ga.num_tiles < sms ? ga.num_tiles : sms));
+  cfg.blockDim = dim3(kNvThreads);
+  cfg.dynamicSmemBytes = kNvSmem;
+  cfg.stream = as_cuda(stream);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, gemm_nvfp4_kernel, ta, to, ga);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return FRT_ERR_CUDA;
+  }
+  note_launches(1);
+  return launch_status();
+}

@@ -342,6 +342,63 @@ def frt_gemm_bf16_next_scale(a, w_packed, N, w_scale=None, bias=None, act_cols=0
     return out, scale
 
 
+# ---------------------------------------------------------------- NVFP4
+
+def frt_nvfp4_scale_bytes(vectors, K):
+    return lib().frt_nvfp4_scale_bytes(vectors, K)
+
+
+def nvfp4_workspace(device=None):
+    """A zero-filled 16-byte workspace for frt_quantize_nvfp4's amax."""
+    return torch.zeros((lib().frt_quantize_nvfp4_workspace_bytes(),), dtype=torch.uint8,
+                       device=device)
+
+
+def frt_quantize_nvfp4(x, blocks_along_rows=False, static_scale=None, q=None, sf=None,
+                       scale=None, workspace=None, stream=None):
+    """NVFP4 codes (two per byte along K), tiled block scales and the tensor
+    scale g of a 2-D bf16/fp32 tensor.  blocks_along_rows=False: x is
+    [M x K] and q [M x K/2]; True: x is a weight [K x N] and q [K/2 x N].
+    Returns (q uint8, sf uint8, scale fp32 [1])."""
+    rows, cols, ldx = _rows_view(x, "x")
+    V, K = (cols, rows) if blocks_along_rows else (rows, cols)
+    qshape = (rows // 2, cols) if blocks_along_rows else (rows, cols // 2)
+    if q is None:
+        q = torch.empty(qshape, dtype=torch.uint8, device=x.device)
+    nsf = lib().frt_nvfp4_scale_bytes(V, K)
+    if sf is None:
+        sf = torch.empty((max(nsf, 1),), dtype=torch.uint8, device=x.device)
+    if scale is None:
+        scale = torch.empty((1,), dtype=torch.float32, device=x.device)
+    if static_scale is None and workspace is None:
+        workspace = nvfp4_workspace(x.device)
+    wsb = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("frt_quantize_nvfp4",
+           lib().frt_quantize_nvfp4(x.data_ptr(), _XDT[x.dtype], rows, cols, ldx,
+                                    1 if blocks_along_rows else 0, _ptr(static_scale),
+                                    q.data_ptr(), sf.data_ptr(), sf.numel(), _ptr(scale),
+                                    _ptr(workspace), wsb, _stream(stream)))
+    return q, sf, scale
+
+
+def frt_gemm_nvfp4(a_q, a_sf, a_scale, w_packed, w_sf, w_scale, N, bias=None, act_cols=0,
+                   out=None, stream=None):
+    """out = bf16(act(g_a g_w sum_k a[m,k] w[k,n] + bias[n])) on NVFP4
+    operands: a_q [M x K/2] codes with tiled scales a_sf and tensor scale
+    a_scale; the weight packed by frt_pack_weights from its [K/2 x N] codes,
+    its tiled scales w_sf and tensor scale w_scale."""
+    M, Kh, lda = _rows_view(a_q, "a_q")
+    K = 2 * Kh
+    out, ldo = _gemm_out(M, N, out, a_q.device)
+    act, act_cols = _act(act_cols, False)
+    _check("frt_gemm_nvfp4",
+           lib().frt_gemm_nvfp4(a_q.data_ptr(), lda, a_sf.data_ptr(), _ptr(a_scale),
+                                w_packed.data_ptr(), w_sf.data_ptr(), _ptr(w_scale), _ptr(bias),
+                                M, N, K, act, act_cols, out.data_ptr(), ldo,
+                                device_status(a_q.device).data_ptr(), _stream(stream)))
+    return out
+
+
 def frt_gate_residual_ada_norm_bf16(residual, output, gate, style, eps=1e-6, normalized=None,
                                     next_gate=None, stream=None):
     """The decoder block boundary: residual <- bf16(residual + output * gate)

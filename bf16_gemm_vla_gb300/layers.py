@@ -47,6 +47,26 @@ def prepare_fp8(w_f32, bias=None, import_fnuz=False):
     return PackedWeight(packed, K, N, "e4m3", s, bias)
 
 
+@dataclass
+class PackedNvfp4:
+    packed: torch.Tensor  # uint8 tile-layout buffer of the [K/2 x N] code bytes
+    sf: torch.Tensor      # uint8 tiled block scales of the N channels
+    g: torch.Tensor       # fp32 [1] tensor scale
+    K: int
+    N: int
+    bias: Optional[torch.Tensor]
+
+
+def prepare_nvfp4(w_f32, bias=None):
+    """Quantize W [K x N] to NVFP4 (blocks of 16 along K, per output channel)
+    and pack its codes for the GEMM."""
+    K, N = w_f32.shape
+    q, sf, g = frt.frt_quantize_nvfp4(w_f32, blocks_along_rows=True)
+    packed = frt.frt_pack_weights(q, "e4m3")
+    torch.cuda.current_stream(packed.device).synchronize()
+    return PackedNvfp4(packed, sf, g, K, N, bias)
+
+
 def prepare_bf16(w, bias=None):
     """Round W (fp32 or bf16) to bf16 and pack it."""
     K, N = w.shape

@@ -357,6 +357,76 @@ frt_status frt_gemm_bf16_next_scale(const void* a, int64_t lda, const void* w_pa
                                     frt_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * NVFP4: 4-bit E2M1 values with block scales ("FlashRT" article, section 7.2
+ * "NVFP4 path" for the pi0.5 encoder FFN, and the use_fp4 / fp4_layers
+ * switches of its load_model listing; the pages give no formula).  Read as:
+ * E2M1 elements (magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6; sign bit; -0 kept),
+ * one E4M3 scale (OCP encoding, sign bit clear) per 16 consecutive elements
+ * along the reduction dimension K, one fp32 scale g per tensor.  For a
+ * tensor x, every step an IEEE fp32 operation rounded to nearest even:
+ *   g    = amax(x) / (6 * 448)  (1 if amax is 0; NaN ignored), or given
+ *   d    = 6 * g
+ *   sb   = E4M3(b / d), b = max |x| over the 16-element block (saturating)
+ *   e    = value(sb) * g
+ *   q_i  = E2M1(x_i / e), round to nearest even, saturating at +-6, the sign
+ *          kept for a value rounding to 0; NaN -> +0; q = 0 where e == 0
+ *   x_i ~= value(q_i) * value(sb) * g
+ *
+ * Codes are stored two per byte along K, element 2i in the low nibble.
+ * Block scales are stored "tiled", the layout the GEMM copies into tensor
+ * memory: for V vectors (rows of an activation, output channels of a
+ * weight), padded to a multiple of 128, the scale of vector v, block j is
+ * byte ((v / 128) * (K / 64) + j / 4) * 512 + 16 * (v % 32)
+ *       + 4 * ((v % 128) / 32) + j % 4;
+ * padded vectors have scale 0.  frt_nvfp4_scale_bytes() is that buffer's
+ * size (0 unless K % 64 == 0).
+ *
+ * frt_quantize_nvfp4: x [rows x cols] (FRT_BF16 or FRT_F32, row stride ldx,
+ *   16-byte aligned, ldx * element size a multiple of 16).
+ *   blocks_along_rows == 0: the vectors are the rows, K = cols (an
+ *     activation [M x K]); q is [rows x cols / 2] bytes.
+ *   blocks_along_rows != 0: the vectors are the columns, K = rows (a weight
+ *     W[K x N]); q is [rows / 2 x cols] bytes (byte (i, n) holds elements
+ *     (2i, n) low and (2i + 1, n) high): pack it for the GEMM with
+ *     frt_pack_weights(q as bytes [K/2 x N], FRT_E4M3_OCP).
+ *   K % 64 == 0 (else FRT_ERR_UNSUPPORTED_SHAPE); q 16-byte aligned.
+ *   sf: device, sf_bytes >= frt_nvfp4_scale_bytes(V, K).
+ *   static_scale: device, g, or NULL to take g from x's amax; scale receives
+ *   g (may be NULL).  workspace: 16 bytes (frt_quantize_nvfp4_workspace_bytes),
+ *   16-byte aligned, zero-filled before its first use and left zero by every
+ *   call; needed when static_scale is NULL; calls sharing it are ordered on
+ *   one stream.  Two launches (amax, encode), one with a static scale.
+ *
+ * frt_gemm_nvfp4: out = bf16(act(acc * (g_a * g_w) + bias[n])) with
+ *   acc[m, n] = sum_k value(qa[m,k]) value(sa[m,k/16]) value(qw[k,n]) value(sw[n,k/16])
+ *   in fp32 on the tensor cores (block-scaled MMA), GELU on the first
+ *   act_cols columns (act FRT_ACT_NONE or FRT_ACT_GELU_TANH).
+ *   a_q: [M x K/2] codes, row stride lda BYTES (lda >= K/2, lda % 16 == 0);
+ *   a_sf: tiled scales of the M rows; a_scale: g_a (1 float, NULL = 1).
+ *   w_packed: frt_pack_weights of the weight's [K/2 x N] code bytes;
+ *   w_sf: tiled scales of the N channels; w_scale: g_w (1 float, NULL = 1).
+ *   bias: N floats or NULL.  out: bf16 [M x N], row stride ldo (ldo % 8 ==
+ *   0).  K % 256 == 0 and N % 16 == 0 (else FRT_ERR_UNSUPPORTED_SHAPE); all
+ *   pointers 16-byte aligned.  The weights are load-time data (as for
+ *   frt_gemm_fp8).  dev_status as for frt_gemm_fp8.  Allocates nothing;
+ *   legal under stream capture.
+ * ---------------------------------------------------------------------- */
+size_t frt_nvfp4_scale_bytes(int64_t vectors, int64_t K);
+
+size_t frt_quantize_nvfp4_workspace_bytes(void);
+
+frt_status frt_quantize_nvfp4(const void* x, frt_dtype x_dtype, int64_t rows, int64_t cols,
+                              int64_t ldx, int blocks_along_rows, const float* static_scale,
+                              uint8_t* q, uint8_t* sf, size_t sf_bytes, float* scale,
+                              void* workspace, size_t workspace_bytes, frt_stream_t stream);
+
+frt_status frt_gemm_nvfp4(const uint8_t* a_q, int64_t lda, const uint8_t* a_sf,
+                          const float* a_scale, const void* w_packed, const uint8_t* w_sf,
+                          const float* w_scale, const float* bias, int64_t M, int64_t N, int64_t K,
+                          frt_act act, int64_t act_cols, void* out, int64_t ldo, int* dev_status,
+                          frt_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * The BF16 decoder block boundary in one kernel ("Real-time VLA inference on
  * AMD hardware", "Fusing the BF16 decoder boundary"), for each row m of an
  * [M x H] tensor:

@@ -160,6 +160,24 @@ def dequantize(q, sb, g):
     return t * s * np.float64(g)
 
 
+def tile_scales(sb):
+    """Block scales sb [V x K/16] in the tiled layout the GEMM reads: vectors
+    padded with zero scales to a multiple of 128; per group of 128 vectors
+    and 4 blocks (64 elements of K) one 512-byte atom of 32 lines x 16 bytes,
+    line i holding vectors i, i + 32, i + 64, i + 96 (4 bytes each, blocks in
+    order); atoms ordered by vector group, then by K.  Returns a flat uint8
+    array."""
+    sb = np.asarray(sb, dtype=np.uint8)
+    V, nb = sb.shape
+    assert nb % 4 == 0
+    vp = -(-V // 128) * 128
+    pad = np.zeros((vp, nb), dtype=np.uint8)
+    pad[:V] = sb
+    # [group g][quarter j][line i][chunk c][block t] -> [g][c][i][j][t]
+    t = pad.reshape(vp // 128, 4, 32, nb // 4, 4)
+    return np.ascontiguousarray(t.transpose(0, 3, 2, 1, 4)).reshape(-1)
+
+
 def pack_nibbles(q):
     """Two codes per byte along K: element 2j in the low nibble of byte j."""
     q = np.asarray(q, dtype=np.uint8)
