@@ -66,6 +66,23 @@ __device__ __forceinline__ uint32_t e2m1_code(float y) {
   return sign | c;
 }
 
+// E2M1 code of the IEEE fp32 quotient x / e, with r = RN(1 / e) a positive
+// normal number (fast).  As for the E4M3 encode of the quantize kernels:
+// RN(x / e) lies within a relative 1.5 * 2^-23 of y = x * r, so inside
+// [y (1 - 2^-20), y (1 + 2^-20)] even after that bracket's own rounding; the
+// code is monotone in the value, so when both ends of the bracket give the
+// same code, so does RN(x / e).  Otherwise (y within a few ulps of a
+// rounding boundary) the IEEE division decides.
+__device__ __forceinline__ uint32_t e2m1_code_div(float x, float e, float r, bool fast) {
+  if (fast) {
+    const float y = x * r;
+    const uint32_t lo = e2m1_code(y * (1.0f - 0x1p-20f));
+    const uint32_t hi = e2m1_code(y * (1.0f + 0x1p-20f));
+    if (lo == hi) return lo;
+  }
+  return e2m1_code(__fdiv_rn(x, e));
+}
+
 // Value of a non-negative OCP E4M3 byte (no NaN: the block scales saturate).
 __device__ __forceinline__ float e4m3_value_pos(uint32_t b) {
   const uint32_t e = (b >> 3) & 15u, m = b & 7u;
@@ -86,17 +103,56 @@ __device__ __forceinline__ float nv_to_f32<__nv_bfloat16>(__nv_bfloat16 v) {
 
 constexpr int kNvQThreads = 256;
 
-template <typename T>
+// Pass 1: max |x| over the tensor (NaN ignored by fmaxf), folded into ws[0].
+// kVec: x is read as 16-byte vectors (cols and ldx multiples of the vector,
+// x 16-byte aligned), four in flight per thread; else element by element.
+template <typename T, bool kVec>
 __global__ void __launch_bounds__(kNvQThreads) nvfp4_amax_kernel(const T* __restrict__ x,
                                                                   int64_t rows, int64_t cols,
                                                                   int64_t ldx, unsigned* ws) {
+  constexpr int VEC = kVec ? 16 / static_cast<int>(sizeof(T)) : 1;
+  constexpr int kU = 4;
   __shared__ float red[kNvQThreads / 32];
   dev::grid_dependency_wait();  // x may come from the previous grid
   float m = 0.0f;
-  for (int64_t r = blockIdx.y; r < rows; r += gridDim.y)
-    for (int64_t c = static_cast<int64_t>(blockIdx.x) * kNvQThreads + threadIdx.x; c < cols;
-         c += static_cast<int64_t>(gridDim.x) * kNvQThreads)
-      m = fmaxf(m, fabsf(nv_to_f32<T>(x[r * ldx + c])));  // NaN is ignored by fmaxf
+  // (the host keeps rows * cols below 2^31: 32-bit index arithmetic)
+  const uint32_t vpr = static_cast<uint32_t>(cols / VEC);
+  const uint32_t total = static_cast<uint32_t>(rows) * vpr;
+  const uint32_t stride = gridDim.x * kNvQThreads;
+  for (uint32_t i0 = blockIdx.x * kNvQThreads + threadIdx.x; i0 < total; i0 += kU * stride) {
+    if constexpr (kVec) {
+      uint4 w[kU];
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const uint32_t i = i0 + u * stride;
+        const uint32_t r = i / vpr, c = i - r * vpr;
+        w[u] = i < total ? __ldg(reinterpret_cast<const uint4*>(x + r * ldx + c * VEC))
+                         : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const uint32_t ww[4] = {w[u].x, w[u].y, w[u].z, w[u].w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          if constexpr (sizeof(T) == 2) {
+            m = fmaxf(m, fabsf(__uint_as_float(ww[k] << 16)));
+            m = fmaxf(m, fabsf(__uint_as_float(ww[k] & 0xFFFF0000u)));
+          } else {
+            m = fmaxf(m, fabsf(__uint_as_float(ww[k])));
+          }
+        }
+      }
+    } else {
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const uint32_t i = i0 + u * stride;
+        if (i < total) {
+          const uint32_t r = i / vpr, c = i - r * vpr;
+          m = fmaxf(m, fabsf(nv_to_f32<T>(x[r * ldx + c])));
+        }
+      }
+    }
+  }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
@@ -133,12 +189,13 @@ __global__ void __launch_bounds__(kNvQThreads) nvfp4_encode_kernel(
   __syncthreads();
   const float g = g_sh;
   const float d = __fmul_rn(6.0f, g);
-  const int64_t nb = Kd / kBlk;             // blocks per vector
-  const int64_t vpad = (V + 127) / 128 * 128;
+  // (the host keeps vpad * nb below 2^31: 32-bit index arithmetic)
+  const uint32_t nb = static_cast<uint32_t>(Kd / kBlk);  // blocks per vector
+  const uint32_t vpad = static_cast<uint32_t>((V + 127) / 128 * 128);
   const int64_t kc_total = Kd / 64;
-  const int64_t total = vpad * nb;
-  for (int64_t t = static_cast<int64_t>(blockIdx.x) * kNvQThreads + threadIdx.x; t < total;
-       t += static_cast<int64_t>(gridDim.x) * kNvQThreads) {
+  const uint32_t total = vpad * nb;
+  for (uint32_t t = blockIdx.x * kNvQThreads + threadIdx.x; t < total;
+       t += gridDim.x * kNvQThreads) {
     int64_t v, j;
     if constexpr (kAlongRows) {  // consecutive threads: consecutive columns (coalesced)
       v = t % vpad;
@@ -175,9 +232,11 @@ __global__ void __launch_bounds__(kNvQThreads) nvfp4_encode_kernel(
       for (int i = 0; i < kBlk; ++i) b = fmaxf(b, fabsf(f[i]));
       sbyte = encode_e4m3<false>(__fdiv_rn(b, d));  // b >= 0, d > 0: a non-negative byte
       const float e = __fmul_rn(e4m3_value_pos(sbyte), g);
+      const float r = __frcp_rn(e);
+      const bool fast = e > 0.0f && (__float_as_uint(r) >> 23) - 1u < 254u;
       uint32_t c[kBlk];
 #pragma unroll
-      for (int i = 0; i < kBlk; ++i) c[i] = e > 0.0f ? e2m1_code(__fdiv_rn(f[i], e)) : 0u;
+      for (int i = 0; i < kBlk; ++i) c[i] = e > 0.0f ? e2m1_code_div(f[i], e, r, fast) : 0u;
       if constexpr (kAlongRows) {
         // [K/2 x V]: byte (8 j + p, v) holds elements 16 j + 2 p (low) and + 1
 #pragma unroll
@@ -467,10 +526,13 @@ frt_status quantize_nvfp4_typed(const T* x, int64_t rows, int64_t cols, int64_t 
   cudaError_t e = cudaSuccess;
   int launches = 1;
   if (!static_scale) {
-    const int gx = static_cast<int>(std::min<int64_t>(ceil_div(cols, kNvQThreads), 64));
-    const int gy = static_cast<int>(std::min<int64_t>(rows, std::max<int64_t>(1, 4 * sms / gx)));
-    cfg.gridDim = dim3(gx, gy);
-    e = cudaLaunchKernelEx(&cfg, nvfp4_amax_kernel<T>, x, rows, cols, ldx, ws);
+    constexpr int VEC = 16 / static_cast<int>(sizeof(T));
+    const bool vec = aligned(x, 16) && cols % VEC == 0 && ldx % VEC == 0;
+    const int64_t units = rows * (vec ? cols / VEC : cols);
+    cfg.gridDim = dim3(static_cast<unsigned>(
+        std::max<int64_t>(1, std::min<int64_t>(ceil_div(units, 4 * kNvQThreads), 4 * sms))));
+    e = vec ? cudaLaunchKernelEx(&cfg, nvfp4_amax_kernel<T, true>, x, rows, cols, ldx, ws)
+            : cudaLaunchKernelEx(&cfg, nvfp4_amax_kernel<T, false>, x, rows, cols, ldx, ws);
     ++launches;
   }
   const int64_t V = along_rows ? cols : rows;
@@ -512,6 +574,8 @@ extern "C" frt_status frt_quantize_nvfp4(const void* x, frt_dtype x_dtype, int64
   const int64_t V = blocks_along_rows ? cols : rows;
   const int64_t Kd = blocks_along_rows ? rows : cols;
   if (Kd % 64 != 0) return FRT_ERR_UNSUPPORTED_SHAPE;
+  if (frt::ceil_div(V, 128) * 128 * (Kd / 16) > (1LL << 31) - 1 || rows * cols > (1LL << 31) - 1)
+    return FRT_ERR_UNSUPPORTED_SHAPE;
   if (sf_bytes < frt_nvfp4_scale_bytes(V, Kd)) return FRT_ERR_WORKSPACE_TOO_SMALL;
   if (!static_scale && (!workspace || workspace_bytes < 16)) return FRT_ERR_WORKSPACE_TOO_SMALL;
   const int esz = x_dtype == FRT_BF16 ? 2 : 4;
