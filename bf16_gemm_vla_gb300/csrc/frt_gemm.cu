@@ -1084,7 +1084,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
     }
     if (early_bye && !bye) dev::cluster_arrive_relaxed();
-    if (lane == 0) dev::bulk_wait_all();  // stores complete before the grid ends
+    // the TMA stores have read their staging buffers before the CTA leaves;
+    // their writes are performed before the grid completes (and before a
+    // dependent grid's wait returns), so the CTA does not wait for them
+    if (lane == 0) dev::bulk_wait_read<0>();
     if (p.s_cols) {
       // the next layer's scale: the CTA's maximum, folded in by one thread
       float m = amax;

@@ -269,17 +269,32 @@ __global__ void __launch_bounds__(kNvQThreads) nvfp4_encode_kernel(
 // ------------------------------------------------------------------ GEMM
 
 constexpr int kNvThreads = 192;  // copy warp, MMA warp, 4 epilogue warps
-constexpr int kNvStages = 4;
-constexpr int kNvTile = 128;
-constexpr int kNvOpBytes = kNvTile * 128;  // codes of one operand per k-block (256 elements)
-constexpr int kNvSfBytes = 4 * 512;        // 4 scale atoms per operand per k-block
-constexpr int kNvStageBytes = 2 * kNvOpBytes + 2 * kNvSfBytes;
-constexpr int kNvOutOff = kNvStages * kNvStageBytes;
-constexpr int kNvBiasOff = kNvOutOff + 4 * 2 * kWarpOutBytes;
-constexpr int kNvBarOff = kNvBiasOff + 2 * kNvTile * 4;
-constexpr int kNvSmem = 1024 + kNvBarOff + 256;
-constexpr uint32_t kNvTmemCols = 512;      // 2 accumulators of 128 columns, then scales
-constexpr uint32_t kNvSfCol0 = 2 * kNvTile;  // per stage: 16 columns A scales, 16 B scales
+constexpr int kNvTile = 128;     // rows of a tile; channels of one half
+constexpr int kNvOpBytes = kNvTile * 128;  // codes of 128 rows per k-block (256 elements)
+constexpr int kNvSfBytes = 4 * 512;        // 4 scale atoms of 128 rows per k-block
+constexpr uint32_t kNvTmemCols = 512;
+
+// A tile is 128 rows x 128 channels: per K step (64 elements) one block-
+// scaled MMA of 128 x 128.  TMEM: two accumulators of 128 columns (a tile's
+// epilogue overlaps the next tile's MMAs), then per stage 16 columns of A
+// scales and 16 of B scales.  (Tiles of 256 channels, two MMAs sharing the
+// activations, were measured no faster: the k-block rate, not the bytes
+// per FLOP, is the limit.)
+struct NvCfg {
+  static constexpr int kHalves = 1;
+  static constexpr int kStages = 4;
+  static constexpr int kStageBytes = (1 + kHalves) * kNvOpBytes + (1 + kHalves) * kNvSfBytes;
+  static constexpr int kOutOff = kStages * kStageBytes;
+  static constexpr int kBiasOff = kOutOff + 4 * 2 * kWarpOutBytes;
+  static constexpr int kBarOff = kBiasOff + 2 * kHalves * kNvTile * 4;
+  static constexpr int kSmem = 1024 + kBarOff + 256;
+  static constexpr int kAccBufs = 2;
+  static constexpr uint32_t kAccCols = kHalves * kNvTile;
+  static constexpr uint32_t kSfCol0 = kAccBufs * kAccCols;
+  static constexpr uint32_t kSfColsPerStage = 16u * (1 + kHalves);
+  static_assert(kSfCol0 + kStages * kSfColsPerStage <= kNvTmemCols, "TMEM budget");
+  static_assert(kSmem <= 232448, "shared memory budget");
+};
 
 struct NvGemmArgs {
   const uint8_t* a_sf;
@@ -298,11 +313,16 @@ struct NvGemmArgs {
 __global__ void __launch_bounds__(kNvThreads, 1)
     gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmap_a,
                       const __grid_constant__ CUtensorMap tmap_out, const NvGemmArgs p) {
+  using C = NvCfg;
+  constexpr int kHalves = C::kHalves;
+  constexpr int kNvStages = C::kStages;
+  constexpr int kNvStageBytes = C::kStageBytes;
+  constexpr int kTileN = kHalves * kNvTile;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = smem_raw + ((1024u - (dev::smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sbase = dev::smem_u32(base);
-  float* bias_s = reinterpret_cast<float*>(base + kNvBiasOff);  // [2 tiles][128 channels]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(base + kNvBarOff);
+  float* bias_s = reinterpret_cast<float*>(base + C::kBiasOff);  // [2 tiles][kTileN channels]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base + C::kBarOff);
   const uint32_t full0 = dev::smem_u32(bars);
   const uint32_t empty0 = full0 + 8 * kNvStages;
   const uint32_t tfull0 = empty0 + 8 * kNvStages;
@@ -365,16 +385,21 @@ __global__ void __launch_bounds__(kNvThreads, 1)
           const uint32_t st = sbase + s * kNvStageBytes;
           const uint32_t fb = full0 + 8 * s;
           dev::mbar_arrive_expect_tx(fb, kNvStageBytes);
+          // stage: A codes, B codes of each half (128 channel rows apiece,
+          // adjacent: one 128 x kTileN operand), A scales, B scales per half
           dev::tma_load_2d(st, &tmap_a, kb * 128, tm * kNvTile, fb, pol_a);
-          dev::bulk_load(st + kNvOpBytes,
-                         p.w_packed + (static_cast<size_t>(tn) * p.kb_total + kb) * kNvOpBytes,
-                         kNvOpBytes, fb, pol_w);
-          dev::bulk_load(st + 2 * kNvOpBytes,
+#pragma unroll
+          for (int h = 0; h < kHalves; ++h) {
+            const size_t nb = static_cast<size_t>(tn) * kHalves + h;
+            dev::bulk_load(st + (1 + h) * kNvOpBytes,
+                           p.w_packed + (nb * p.kb_total + kb) * kNvOpBytes, kNvOpBytes, fb,
+                           pol_w);
+            dev::bulk_load(st + (1 + kHalves) * kNvOpBytes + (1 + h) * kNvSfBytes,
+                           p.w_sf + (nb * p.kc_total + 4 * kb) * 512, kNvSfBytes, fb, pol_w);
+          }
+          dev::bulk_load(st + (1 + kHalves) * kNvOpBytes,
                          p.a_sf + (static_cast<size_t>(tm) * p.kc_total + 4 * kb) * 512,
                          kNvSfBytes, fb, pol_a);
-          dev::bulk_load(st + 2 * kNvOpBytes + kNvSfBytes,
-                         p.w_sf + (static_cast<size_t>(tn) * p.kc_total + 4 * kb) * 512,
-                         kNvSfBytes, fb, pol_w);
           ++issued;
           if (++s == kNvStages) {
             s = 0;
@@ -395,13 +420,13 @@ __global__ void __launch_bounds__(kNvThreads, 1)
       uint32_t ph = 0;
       bool stop = false;
       for (int it = 0; it < my_tiles && !stop; ++it) {
-        const int b = it & 1;
-        const uint32_t u = static_cast<uint32_t>(it >> 1);
+        const int b = it % C::kAccBufs;
+        const uint32_t u = static_cast<uint32_t>(it / C::kAccBufs);
         if (!dev::mbar_wait(tempty0 + 8 * b, (u & 1) ^ 1, abort_flag, p.dev_status,
                             dev::kTimeoutMma))
           break;
         dev::tc_fence_after();
-        const uint32_t d = tmem + static_cast<uint32_t>(b * kNvTile);
+        const uint32_t d = tmem + static_cast<uint32_t>(b) * C::kAccCols;
         for (int kb = 0; kb < p.kb_total; ++kb) {
           if (!dev::mbar_wait(full0 + 8 * s, ph & 1, abort_flag, p.dev_status, dev::kTimeoutMma)) {
             stop = true;
@@ -409,19 +434,28 @@ __global__ void __launch_bounds__(kNvThreads, 1)
           }
           dev::tc_fence_after();
           const uint32_t st = sbase + s * kNvStageBytes;
+          const uint32_t sf_st = st + (1 + kHalves) * kNvOpBytes;  // A scales, then B per half
           const uint64_t ad = dev::smem_desc_sw128(st);
-          const uint64_t bd = dev::smem_desc_sw128(st + kNvOpBytes);
-          const uint32_t sfa = tmem + kNvSfCol0 + 32u * s;  // 16 columns of A scales,
-          const uint32_t sfb = sfa + 16u;                    // then 16 of B scales
+          // 16 columns of A scales, then 16 of B scales per half
+          const uint32_t sfa = tmem + C::kSfCol0 + C::kSfColsPerStage * s;
+          // the k-block's scale atoms first (copies and MMAs run in issue
+          // order), then its MMAs back to back
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
-            dev::tmem_cp_32x128b_x4(sfa + 4u * k,
-                                    dev::smem_desc_noswz(st + 2 * kNvOpBytes + 512 * k, 128, 128));
-            dev::tmem_cp_32x128b_x4(
-                sfb + 4u * k,
-                dev::smem_desc_noswz(st + 2 * kNvOpBytes + kNvSfBytes + 512 * k, 128, 128));
-            dev::mma_nvfp4(d, ad + 2 * k, bd + 2 * k, idesc, sfa + 4u * k, sfb + 4u * k,
-                           (kb | k) != 0);
+            dev::tmem_cp_32x128b_x4(sfa + 4u * k, dev::smem_desc_noswz(sf_st + 512 * k, 128, 128));
+#pragma unroll
+            for (int h = 0; h < kHalves; ++h)
+              dev::tmem_cp_32x128b_x4(
+                  sfa + 16u * (1 + h) + 4u * k,
+                  dev::smem_desc_noswz(sf_st + (1 + h) * kNvSfBytes + 512 * k, 128, 128));
+          }
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+#pragma unroll
+            for (int h = 0; h < kHalves; ++h)
+              dev::mma_nvfp4(d + h * kNvTile, ad + 2 * k,
+                             dev::smem_desc_sw128(st + (1 + h) * kNvOpBytes) + 2 * k, idesc,
+                             sfa + 4u * k, sfa + 16u * (1 + h) + 4u * k, (kb | k) != 0);
           }
           dev::mma_commit(empty0 + 8 * s);
           if (++s == kNvStages) {
@@ -437,37 +471,38 @@ __global__ void __launch_bounds__(kNvThreads, 1)
     const int et = threadIdx.x - 64;
     const int ew = warp & 3;  // TMEM lane quarter
     const uint32_t lane_off = static_cast<uint32_t>(ew * 32) << 16;
-    uint8_t* wbuf = base + kNvOutOff + (warp - 2) * 2 * kWarpOutBytes;
-    const uint32_t wbuf_s = sbase + kNvOutOff + (warp - 2) * 2 * kWarpOutBytes;
+    uint8_t* wbuf = base + C::kOutOff + (warp - 2) * 2 * kWarpOutBytes;
+    const uint32_t wbuf_s = sbase + C::kOutOff + (warp - 2) * 2 * kWarpOutBytes;
     int wb = 0;
     bool ok = dev::mbar_wait(scale_bar, 0, abort_flag, p.dev_status, dev::kTimeoutEpilogue);
     const float gs = *gscale_s;
     for (int it = 0; it < my_tiles && ok; ++it) {
       const int t = first + it * step;
       const int tm = t % p.tiles_m, tn = t / p.tiles_m;
-      const int b = it & 1;
-      const uint32_t u = static_cast<uint32_t>(it >> 1);
-      float* bs = bias_s + (it & 1) * kNvTile;
-      {
-        const int n = tn * kNvTile + et;
-        bs[et] = (p.bias && n < p.N) ? __ldg(p.bias + n) : 0.0f;
+      const int b = it % C::kAccBufs;
+      const uint32_t u = static_cast<uint32_t>(it / C::kAccBufs);
+      float* bs = bias_s + (it & 1) * kTileN;
+#pragma unroll
+      for (int h = 0; h < kHalves; ++h) {
+        const int n = tn * kTileN + h * kNvTile + et;
+        bs[h * kNvTile + et] = (p.bias && n < p.N) ? __ldg(p.bias + n) : 0.0f;
       }
       dev::named_sync(1, 128);
       ok = dev::mbar_wait(tfull0 + 8 * b, u & 1, abort_flag, p.dev_status, dev::kTimeoutEpilogue);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       dev::tc_fence_after();
-      const uint32_t tacc = tmem + lane_off + static_cast<uint32_t>(b * kNvTile);
+      const uint32_t tacc = tmem + lane_off + static_cast<uint32_t>(b) * C::kAccCols;
 #pragma unroll 1
-      for (int c = 0; c < kNvTile; c += 32) {
+      for (int c = 0; c < kTileN; c += 32) {
         float v[32];
         dev::tmem_ld32(tacc + c, v);
-        if (c + 32 == kNvTile) {  // accumulator read out: back to the MMA thread
+        if (c + 32 == kTileN) {  // accumulator read out: back to the MMA thread
           dev::tc_fence_before();
           __syncwarp();
           if (lane == 0) dev::mbar_arrive(tempty0 + 8 * b);
         }
-        const int n0 = tn * kNvTile + c;
+        const int n0 = tn * kTileN + c;
 #pragma unroll
         for (int j = 0; j < 32; ++j) v[j] = lin(v[j], gs, bs[c + j]);
         if (n0 + 32 <= p.act_cols) {
@@ -480,12 +515,16 @@ __global__ void __launch_bounds__(kNvThreads, 1)
             v[j] = n0 + j < p.act_cols ? gv : v[j];
           }
         }
-        warp_store<false, 32>(v, wbuf + wb * kWarpOutBytes, wbuf_s + wb * kWarpOutBytes,
-                              &tmap_out, n0, tm * kNvTile + ew * 32, lane);
+        if (n0 < p.N)
+          warp_store<false, 32>(v, wbuf + wb * kWarpOutBytes, wbuf_s + wb * kWarpOutBytes,
+                                &tmap_out, n0, tm * kNvTile + ew * 32, lane);
         wb ^= 1;
       }
     }
-    if (lane == 0) dev::bulk_wait_all();  // stores complete before the grid ends
+    // the TMA stores have read their staging buffers before the CTA leaves;
+    // their writes are performed before the grid completes (and before a
+    // dependent grid's wait returns), so the CTA does not wait for them
+    if (lane == 0) dev::bulk_wait_read<0>();
   }
   dev::tc_fence_before();
   __syncthreads();
@@ -502,12 +541,30 @@ cudaError_t prepare_nvfp4_gemm() {
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(mu);
   if (!set[dev]) {
-    const cudaError_t e = cudaFuncSetAttribute(
-        gemm_nvfp4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kNvSmem);
+    const cudaError_t e =
+        cudaFuncSetAttribute(gemm_nvfp4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             NvCfg::kSmem);
     if (e != cudaSuccess) return e;
     set[dev] = true;
   }
   return cudaSuccess;
+}
+
+cudaError_t launch_nvfp4(const CUtensorMap& ta, const CUtensorMap& to, const NvGemmArgs& ga,
+                         int sms, cudaStream_t stream) {
+  cudaError_t e = prepare_nvfp4_gemm();
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(ga.num_tiles < sms ? ga.num_tiles : sms));
+  cfg.blockDim = dim3(kNvThreads);
+  cfg.dynamicSmemBytes = NvCfg::kSmem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, gemm_nvfp4_kernel, ta, to, ga);
 }
 
 template <typename T>
@@ -651,22 +708,10 @@ extern "C" frt_status frt_gemm_nvfp4(const uint8_t* a_q, int64_t lda, const uint
   ga.kb_total = static_cast<int>(K / 256);
   ga.kc_total = static_cast<int>(K / 64);
   ga.tiles_m = static_cast<int>(ceil_div(M, kNvTile));
-  ga.num_tiles = ga.tiles_m * static_cast<int>(ceil_div(N, kNvTile));
   ga.dev_status = dev_status;
-  cudaError_t e = prepare_nvfp4_gemm();
-  if (e != cudaSuccess) return FRT_ERR_CUDA;
   const int sms = sm_count() > 0 ? sm_count() : 148;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(ga.num_tiles < sms ? ga.num_tiles : sms));
-  cfg.blockDim = dim3(kNvThreads);
-  cfg.dynamicSmemBytes = kNvSmem;
-  cfg.stream = as_cuda(stream);
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, gemm_nvfp4_kernel, ta, to, ga);
+  ga.num_tiles = static_cast<int>(ga.tiles_m * ceil_div(N, kNvTile));
+  const cudaError_t e = launch_nvfp4(ta, to, ga, sms, as_cuda(stream));
   if (e != cudaSuccess) {
     cudaGetLastError();
     return FRT_ERR_CUDA;
