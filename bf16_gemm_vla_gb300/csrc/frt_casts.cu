@@ -102,6 +102,38 @@ __device__ __forceinline__ void load8<float>(const float* p, float (&f)[8]) {
   f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
 }
 
+// 8 consecutive elements of a row as loaded (16 bytes of bf16, 32 of fp32),
+// converted to fp32 after all of a thread's loads are in flight.
+template <typename T>
+struct Raw8;
+template <>
+struct Raw8<__nv_bfloat16> {
+  uint4 v;
+  __device__ __forceinline__ void load(const __nv_bfloat16* p) {
+    v = __ldg(reinterpret_cast<const uint4*>(p));
+  }
+  __device__ __forceinline__ void unpack(float (&f)[8]) const {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      f[2 * i] = __uint_as_float(w[i] << 16);
+      f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+  }
+};
+template <>
+struct Raw8<float> {
+  float4 a, b;
+  __device__ __forceinline__ void load(const float* p) {
+    a = __ldg(reinterpret_cast<const float4*>(p));
+    b = __ldg(reinterpret_cast<const float4*>(p) + 1);
+  }
+  __device__ __forceinline__ void unpack(float (&f)[8]) const {
+    f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+    f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+  }
+};
+
 __device__ __forceinline__ float block_max(float v, float* red) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
@@ -228,38 +260,48 @@ __global__ void __launch_bounds__(kQThreads) encode_tensor_kernel(
   auto xoffset = [&](int64_t i) -> int64_t {  // element offset of vector i (walk at i)
     return dense ? i * VEC : walk.offset() * VEC;
   };
-  for (int64_t i0 = first; i0 < total; i0 += kUnroll * stride) {
-    if constexpr (VEC == 8) {
-      float f[kUnroll][8];
+  if constexpr (VEC == 8) {
+    // U loads of 8 elements in flight per thread (raw), then the encodes
+    constexpr int U = sizeof(T) == 2 ? 6 : 4;
+    auto body = [&](int64_t i0) {
+      Raw8<T> v[U];
 #pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
+      for (int u = 0; u < U; ++u) {
         const int64_t i = i0 + u * stride;
-        if (i < total) load8<T>(x + xoffset(i), f[u]);
+        if (i < total) v[u].load(x + xoffset(i));
         if (!dense) walk.next();
       }
 #pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
+      for (int u = 0; u < U; ++u) {
         const int64_t i = i0 + u * stride;
         if (i >= total) break;
-        uint32_t lo = 0, hi = 0;
+        float f[8];
+        v[u].unpack(f);
+        uint2 w;
         if constexpr (kFnuz) {
+          w = make_uint2(0u, 0u);
 #pragma unroll
-          for (int e = 0; e < 4; ++e) lo |= quantize_one<true>(f[u][e], s, r, fast_ok) << (8 * e);
+          for (int e = 0; e < 4; ++e) w.x |= quantize_one<true>(f[e], s, r, fast_ok) << (8 * e);
 #pragma unroll
-          for (int e = 0; e < 4; ++e)
-            hi |= quantize_one<true>(f[u][4 + e], s, r, fast_ok) << (8 * e);
+          for (int e = 0; e < 4; ++e) w.y |= quantize_one<true>(f[4 + e], s, r, fast_ok) << (8 * e);
         } else {
-          lo = quantize_pair_ocp(f[u][0], f[u][1], s, r, fast_ok) |
-               (quantize_pair_ocp(f[u][2], f[u][3], s, r, fast_ok) << 16);
-          hi = quantize_pair_ocp(f[u][4], f[u][5], s, r, fast_ok) |
-               (quantize_pair_ocp(f[u][6], f[u][7], s, r, fast_ok) << 16);
-          lo = canonical_nan_x4(lo);
-          hi = canonical_nan_x4(hi);
+          w = encode8_ocp(f, s, r, fast_ok);
         }
         // q is dense: element (r, c) at r * cols + c = i * VEC
-        *reinterpret_cast<uint2*>(q + i * VEC) = make_uint2(lo, hi);
+        *reinterpret_cast<uint2*>(q + i * VEC) = w;
       }
+    };
+    const int64_t span = U * stride;
+    if (dense && !static_scale) {
+      // the amax pass read x in the same grid-stride order: its last reads
+      // are the ones still in L2, so this pass takes its spans last first
+      for (int64_t j = first < total ? (total - first - 1) / span : -1; j >= 0; --j)
+        body(first + j * span);
     } else {
+      for (int64_t i0 = first; i0 < total; i0 += span) body(i0);
+    }
+  } else {
+    for (int64_t i0 = first; i0 < total; i0 += kUnroll * stride) {
 #pragma unroll
       for (int u = 0; u < kUnroll; ++u) {
         const int64_t i = i0 + u * stride;

@@ -290,6 +290,20 @@ __device__ __forceinline__ void named_sync(uint32_t id, uint32_t count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
+// Named barrier that also ANDs a predicate over the `count` threads: every
+// participant gets the same answer (a decision to leave a loop that the
+// threads take together).
+__device__ __forceinline__ bool named_all(uint32_t id, uint32_t count, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(count)
+      : "memory");
+  return r != 0;
+}
+
 // ---------------------------------------------------------------- programmatic dependent launch
 
 // Blocks until every grid this one depends on (launched before it on the
@@ -463,6 +477,26 @@ __device__ __forceinline__ void mma_pair(uint32_t tmem_d, uint64_t adesc, uint64
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
   }
+}
+
+// tmem_cp_32x128b_x4 for a CTA pair, issued by the leader: each CTA's shared
+// memory at the descriptor's address goes into that CTA's TMEM at `taddr`.
+__device__ __forceinline__ void tmem_cp_32x128b_x4_pair(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
+               : "memory");
+}
+
+// mma_nvfp4 with M = 256 on a CTA pair: A rows and B columns as mma_pair,
+// each CTA's scales read from its own TMEM at tsfa / tsfb.
+__device__ __forceinline__ void mma_nvfp4_pair(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
+                                               uint32_t idesc, uint32_t tsfa, uint32_t tsfb,
+                                               uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, "
+      "[%5], [%6], p;\n\t}" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(tsfa), "r"(tsfb)
+      : "memory");
 }
 
 // Arrives once on the mbarrier at offset `bar` of every CTA in `cta_mask`

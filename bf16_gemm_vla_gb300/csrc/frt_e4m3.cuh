@@ -138,10 +138,60 @@ __device__ __forceinline__ uint32_t quantize_pair_ocp(float a, float b, float s,
   return encode_e4m3<false>(__fdiv_rn(a, s)) | (encode_e4m3<false>(__fdiv_rn(b, s)) << 8);
 }
 
+
 // NaN bytes (S.1111.111) of four OCP codes -> the positive NaN 0x7f.
 __device__ __forceinline__ uint32_t canonical_nan_x4(uint32_t w) {
   const uint32_t t = (w & 0x7F7F7F7Fu) + 0x01010101u;  // bit 7 set where low 7 bits are 0x7f
   return w & ~(t & 0x80808080u);
+}
+
+// The elements of a vector whose bracket straddles a rounding midpoint (or
+// all of them when the reciprocal is not normal): bytes where the bracket
+// ends' codes lo_d/lo_u (elements 0-3) and hi_d/hi_u (4-7) differ take the
+// IEEE division.  Out of line: rare, and kept out of the hot loop's code.
+__device__ __noinline__ uint2 encode8_ocp_slow(float f0, float f1, float f2, float f3, float f4,
+                                               float f5, float f6, float f7, float s,
+                                               uint32_t lo_d, uint32_t lo_u, uint32_t hi_d,
+                                               uint32_t hi_u, bool all) {
+  const float f[8] = {f0, f1, f2, f3, f4, f5, f6, f7};
+  uint32_t w[2] = {lo_d, hi_d};
+  const uint32_t x[2] = {lo_d ^ lo_u, hi_d ^ hi_u};
+#pragma unroll
+  for (int h = 0; h < 2; ++h)
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      if (all || ((x[h] >> (8 * e)) & 0xFFu)) {
+        const uint32_t c = encode_e4m3<false>(__fdiv_rn(f[4 * h + e], s));
+        w[h] = (w[h] & ~(0xFFu << (8 * e))) | (c << (8 * e));
+      }
+  return make_uint2(canonical_nan_x4(w[0]), canonical_nan_x4(w[1]));
+}
+
+// OCP E4M3 bytes of the IEEE fp32 quotients f[e] / s of 8 elements (element
+// e in byte e % 4 of word e / 4), by the bracket of quantize_pair_ocp with
+// one test for the whole vector; NaN bytes canonical.
+__device__ __forceinline__ uint2 encode8_ocp(const float (&f)[8], float s, float r,
+                                             bool fast_ok) {
+  if (fast_ok) {
+    const unsigned long long rr = f32x2(r, r);
+    const float kDown = 1.0f - 0x1p-20f, kUp = 1.0f + 0x1p-20f;
+    const unsigned long long dn = f32x2(kDown, kDown), up = f32x2(kUp, kUp);
+    uint32_t d[4], u[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const unsigned long long y = mul_f32x2(f32x2(f[2 * k], f[2 * k + 1]), rr);
+      d[k] = cvt_e4m3x2_ocp(mul_f32x2(y, dn));
+      u[k] = cvt_e4m3x2_ocp(mul_f32x2(y, up));
+    }
+    const uint32_t lo_d = d[0] | (d[1] << 16), hi_d = d[2] | (d[3] << 16);
+    const uint32_t lo_u = u[0] | (u[1] << 16), hi_u = u[2] | (u[3] << 16);
+    if (((lo_d ^ lo_u) | (hi_d ^ hi_u)) == 0u)
+      return make_uint2(canonical_nan_x4(lo_d), canonical_nan_x4(hi_d));
+    return encode8_ocp_slow(f[0], f[1], f[2], f[3], f[4], f[5], f[6], f[7], s, lo_d, lo_u, hi_d,
+                            hi_u, false);
+  }
+  return encode8_ocp_slow(f[0], f[1], f[2], f[3], f[4], f[5], f[6], f[7], s, 0u, 0u, 0u, 0u,
+                          true);
 }
 
 __device__ __forceinline__ bool recip_is_normal(float s, float r) {

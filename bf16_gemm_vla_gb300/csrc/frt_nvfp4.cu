@@ -474,7 +474,10 @@ __global__ void __launch_bounds__(kNvThreads, 1)
     uint8_t* wbuf = base + C::kOutOff + (warp - 2) * 2 * kWarpOutBytes;
     const uint32_t wbuf_s = sbase + C::kOutOff + (warp - 2) * 2 * kWarpOutBytes;
     int wb = 0;
-    bool ok = dev::mbar_wait(scale_bar, 0, abort_flag, p.dev_status, dev::kTimeoutEpilogue);
+    // the four warps leave the tile loop together (named_all), so none is
+    // left alone at a named barrier
+    bool ok = dev::named_all(
+        1, 128, dev::mbar_wait(scale_bar, 0, abort_flag, p.dev_status, dev::kTimeoutEpilogue));
     const float gs = *gscale_s;
     for (int it = 0; it < my_tiles && ok; ++it) {
       const int t = first + it * step;
@@ -487,9 +490,8 @@ __global__ void __launch_bounds__(kNvThreads, 1)
         const int n = tn * kTileN + h * kNvTile + et;
         bs[h * kNvTile + et] = (p.bias && n < p.N) ? __ldg(p.bias + n) : 0.0f;
       }
-      dev::named_sync(1, 128);
-      ok = dev::mbar_wait(tfull0 + 8 * b, u & 1, abort_flag, p.dev_status, dev::kTimeoutEpilogue);
-      ok = __all_sync(0xffffffffu, ok);
+      ok = dev::named_all(1, 128, dev::mbar_wait(tfull0 + 8 * b, u & 1, abort_flag, p.dev_status,
+                                                 dev::kTimeoutEpilogue));
       if (!ok) break;
       dev::tc_fence_after();
       const uint32_t tacc = tmem + lane_off + static_cast<uint32_t>(b) * C::kAccCols;
@@ -534,16 +536,334 @@ __global__ void __launch_bounds__(kNvThreads, 1)
   }
 }
 
-cudaError_t prepare_nvfp4_gemm() {
-  static std::mutex mu;
-  static bool set[64] = {false};
+// Pair tiles (more than 128 rows): 256 rows x kBN channels on a CTA pair
+// (cta_group::2).  Each CTA holds 128 rows of A and their scales, half of
+// the tile's channels of B, and the B scales of all kBN channels (each
+// CTA's accumulator has the tile's kBN columns); per K step the even CTA
+// issues one MMA of M = 256, N = kBN, and one scale copy per atom that takes
+// each CTA's shared memory into its own TMEM.  Every copy of both CTAs
+// completes on the leader's full barrier.  kBN = 256 leaves TMEM room for
+// one accumulator only (its epilogue does not overlap the next tile's MMAs);
+// kBN = 128 keeps two.
+template <int kBN>
+struct NvPairCfg {
+  static constexpr int kGroups = kBN / kNvTile;  // 128-channel groups of a tile
+  static constexpr int kAccBufs = kGroups == 2 ? 1 : 2;
+  static constexpr int kStages = kGroups == 2 ? 5 : 6;
+  static constexpr int kABytes = kNvOpBytes;     // 128 rows x 128 bytes
+  static constexpr int kBBytes = kBN / 2 * 128;  // this CTA's channels x 128 bytes
+  static constexpr int kSfaOff = kABytes + kBBytes;
+  static constexpr int kSfbOff = kSfaOff + kNvSfBytes;
+  static constexpr int kStageBytes = kSfbOff + kGroups * kNvSfBytes;
+  static constexpr int kOutOff = kStages * kStageBytes;
+  static constexpr int kBiasOff = kOutOff + 4 * 2 * kWarpOutBytes;
+  static constexpr int kBarOff = kBiasOff + 2 * kBN * 4;
+  static constexpr int kSmem = 1024 + kBarOff + 256;
+  static constexpr uint32_t kAccCols = kBN;
+  static constexpr uint32_t kSfCol0 = kAccBufs * kAccCols;
+  static constexpr uint32_t kSfbCols = 4 * kGroups;  // B scale columns per K step
+  static constexpr uint32_t kSfColsPerStage = 16 + 4 * kSfbCols;
+  static_assert(kStageBytes % 1024 == 0, "stages keep the 128-byte swizzle's alignment");
+  static_assert(kSfCol0 + kStages * kSfColsPerStage <= kNvTmemCols, "TMEM budget");
+  static_assert(kSmem <= 232448, "shared memory budget");
+};
+
+template <int kBN>
+__global__ void __launch_bounds__(kNvThreads, 1)
+    gemm_nvfp4_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                           const __grid_constant__ CUtensorMap tmap_w,
+                           const __grid_constant__ CUtensorMap tmap_sfa,
+                           const __grid_constant__ CUtensorMap tmap_sfb,
+                           const __grid_constant__ CUtensorMap tmap_out, const NvGemmArgs p) {
+  using C = NvPairCfg<kBN>;
+  constexpr int kS = C::kStages;
+  constexpr int kG = C::kGroups;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = smem_raw + ((1024u - (dev::smem_u32(smem_raw) & 1023u)) & 1023u);
+  const uint32_t sbase = dev::smem_u32(base);
+  float* bias_s = reinterpret_cast<float*>(base + C::kBiasOff);  // [2 tiles][kBN channels]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base + C::kBarOff);
+  const uint32_t full0 = dev::smem_u32(bars);
+  const uint32_t empty0 = full0 + 8 * kS;
+  const uint32_t tfull0 = empty0 + 8 * kS;
+  const uint32_t tempty0 = tfull0 + 16;
+  const uint32_t scale_bar = tempty0 + 16;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kS + 5);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float* gscale_s = reinterpret_cast<float*>(tmem_slot + 2);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t crank = dev::cluster_ctarank();
+  const int px = static_cast<int>(crank & 1u);  // CTA within the pair
+  const bool leader = px == 0;
+  const uint32_t lead_rank = crank & ~1u;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kS; ++s) {
+      dev::mbar_init(full0 + 8 * s, 1);
+      dev::mbar_init(empty0 + 8 * s, 1);
+    }
+    dev::mbar_init(tfull0, 1);
+    dev::mbar_init(tfull0 + 8, 1);
+    // an accumulator is released by the epilogue warps of both CTAs
+    dev::mbar_init(tempty0, 8);
+    dev::mbar_init(tempty0 + 8, 8);
+    dev::mbar_init(scale_bar, 1);
+    *abort_flag = 0;
+    dev::fence_mbar_init();
+    dev::prefetch_tmap(&tmap_a);
+    dev::prefetch_tmap(&tmap_w);
+    dev::prefetch_tmap(&tmap_sfa);
+    dev::prefetch_tmap(&tmap_sfb);
+    dev::prefetch_tmap(&tmap_out);
+  }
+  if (warp == 1) dev::tmem_alloc_pair(dev::smem_u32(tmem_slot), kNvTmemCols);
+  dev::tc_fence_before();
+  __syncthreads();
+  dev::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  dev::grid_launch_dependents();
+  // both CTAs' barriers are initialised (published by fence.mbarrier_init)
+  // before either signals the other's; every cluster-barrier arrive and wait
+  // below is executed by all 32 lanes of a warp together
+  dev::cluster_arrive_relaxed();
+  dev::cluster_wait();
+
+  const int first = static_cast<int>(blockIdx.x >> 1);
+  const int step = static_cast<int>(gridDim.x >> 1);
+  const int my_tiles = first < p.num_tiles ? (p.num_tiles - first + step - 1) / step : 0;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ copies
+      const uint64_t pol_w = dev::policy_evict_normal();
+      const uint64_t pol_a = dev::policy_evict_last();
+      struct Cur {
+        int it, kb, tm, tn;
+      };
+      auto set_tile = [&](Cur& c) {
+        const int t = first + c.it * step;
+        c.tm = t % p.tiles_m;
+        c.tn = t / p.tiles_m;
+      };
+      auto advance = [&](Cur& c) {
+        if (++c.kb == p.kb_total) {
+          c.kb = 0;
+          if (++c.it < my_tiles) set_tile(c);
+        }
+      };
+      auto full_bar = [&](int s) { return dev::map_to_rank(full0 + 8 * s, lead_rank); };
+      // static data: this CTA's half of the tile's channels of the weight
+      // k-tile (64 rows of the tile's group, or the CTA's own group of 128)
+      // and the scales of all kBN channels (the leader arms the stage for
+      // both CTAs' bytes)
+      auto load_w = [&](const Cur& c, int s) {
+        const uint32_t st = sbase + s * C::kStageBytes;
+        if (leader) dev::mbar_arrive_expect_tx(full0 + 8 * s, 2u * C::kStageBytes);
+        const int grp = kG * c.tn + (kG == 2 ? px : 0);
+        dev::tma_load_3d_pair(st + C::kABytes, &tmap_w, 0, kG == 2 ? 0 : px * (kNvTile / 2),
+                              grp * p.kb_total + c.kb, full_bar(s), pol_w);
+#pragma unroll
+        for (int g = 0; g < kG; ++g)
+          dev::tma_load_2d_pair(st + C::kSfbOff + g * kNvSfBytes, &tmap_sfb, 0,
+                                ((kG * c.tn + g) * p.kc_total + 4 * c.kb) * 2, full_bar(s),
+                                pol_w);
+      };
+      // the previous grid's data: this CTA's 128 rows and their scales
+      auto load_a = [&](const Cur& c, int s) {
+        const uint32_t st = sbase + s * C::kStageBytes;
+        dev::tma_load_2d_pair(st, &tmap_a, c.kb * 128, c.tm * 2 * kNvTile + px * kNvTile,
+                              full_bar(s), pol_a);
+        dev::tma_load_2d_pair(st + C::kSfaOff, &tmap_sfa, 0,
+                              ((2 * c.tm + px) * p.kc_total + 4 * c.kb) * 2, full_bar(s), pol_a);
+      };
+      const int total = my_tiles * p.kb_total;
+      const int npre = total < kS ? total : kS;
+      Cur start = {0, 0, 0, 0};
+      if (my_tiles > 0) set_tile(start);
+      Cur cur = start;
+      for (int g = 0; g < npre; ++g) {  // first use of each stage needs no wait
+        load_w(cur, g);
+        advance(cur);
+      }
+      dev::grid_dependency_wait();
+      cur = start;
+      for (int g = 0; g < npre; ++g) {
+        load_a(cur, g);
+        advance(cur);
+      }
+      *gscale_s = __fmul_rn(p.a_scale ? __ldcg(p.a_scale) : 1.0f,
+                            p.w_scale ? __ldcg(p.w_scale) : 1.0f);
+      dev::mbar_arrive(scale_bar);
+      int issued = npre;
+      int s = npre % kS;
+      uint32_t ph = static_cast<uint32_t>(npre / kS);
+      for (int g = npre; g < total; ++g) {
+        if (!dev::mbar_wait(empty0 + 8 * s, (ph & 1) ^ 1, abort_flag, p.dev_status,
+                            dev::kTimeoutProducer))
+          break;
+        load_w(cur, s);
+        load_a(cur, s);
+        advance(cur);
+        issued = g + 1;
+        if (++s == kS) {
+          s = 0;
+          ++ph;
+        }
+      }
+      // no copies in flight when the CTA leaves: the copies complete on the
+      // leader's barriers, so wait (bounded, even after an abort) until the
+      // MMAs released the last use of every stage armed
+      for (int g = issued - kS < 0 ? 0 : issued - kS; g < issued; ++g)
+        dev::mbar_wait(empty0 + 8 * (g % kS), (g / kS) & 1, nullptr, p.dev_status,
+                       dev::kTimeoutProducer);
+    }
+    __syncwarp();
+    dev::cluster_arrive_relaxed();
+  } else if (warp == 1) {
+    if (lane == 0 && leader) {
+      // ------------------------------------------------------------ scales + MMA
+      constexpr uint32_t idesc = dev::instr_desc_nvfp4(2 * kNvTile, kBN);
+      const uint16_t pair_mask = static_cast<uint16_t>(3u << lead_rank);
+      int s = 0;
+      uint32_t ph = 0;
+      bool stop = false;
+      for (int it = 0; it < my_tiles && !stop; ++it) {
+        const int b = it % C::kAccBufs;
+        const uint32_t u = static_cast<uint32_t>(it / C::kAccBufs);
+        if (!dev::mbar_wait_cluster(tempty0 + 8 * b, (u & 1) ^ 1, abort_flag, p.dev_status,
+                                    dev::kTimeoutMma))
+          break;
+        dev::tc_fence_after();
+        const uint32_t d = tmem + static_cast<uint32_t>(b) * C::kAccCols;
+        for (int kb = 0; kb < p.kb_total; ++kb) {
+          if (!dev::mbar_wait(full0 + 8 * s, ph & 1, abort_flag, p.dev_status, dev::kTimeoutMma)) {
+            stop = true;
+            break;
+          }
+          dev::tc_fence_after();
+          const uint32_t st = sbase + s * C::kStageBytes;
+          const uint32_t sfa = tmem + C::kSfCol0 + C::kSfColsPerStage * s;
+          const uint32_t sfb = sfa + 16;
+          // the k-block's scale atoms (copies and MMAs run in issue order),
+          // then its MMAs; per K step 4 columns of A scales and kSfbCols of B
+          // scales, channel n of the tile in column n / 32 (one atom per
+          // 128-channel group)
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            dev::tmem_cp_32x128b_x4_pair(sfa + 4u * k,
+                                         dev::smem_desc_noswz(st + C::kSfaOff + 512 * k, 128, 128));
+#pragma unroll
+            for (int g = 0; g < kG; ++g)
+              dev::tmem_cp_32x128b_x4_pair(
+                  sfb + C::kSfbCols * k + 4u * g,
+                  dev::smem_desc_noswz(st + C::kSfbOff + g * kNvSfBytes + 512 * k, 128, 128));
+          }
+          const uint64_t ad = dev::smem_desc_sw128(st);
+          const uint64_t bd = dev::smem_desc_sw128(st + C::kABytes);
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            dev::mma_nvfp4_pair(d, ad + 2 * k, bd + 2 * k, idesc, sfa + 4u * k,
+                                sfb + C::kSfbCols * k, (kb | k) != 0);
+          dev::mma_commit_pair(empty0 + 8 * s, pair_mask);
+          if (++s == kS) {
+            s = 0;
+            ++ph;
+          }
+        }
+        dev::mma_commit_pair(tfull0 + 8 * b, pair_mask);
+      }
+    }
+    __syncwarp();
+    dev::cluster_arrive_relaxed();
+  } else {
+    // -------------------------------------------------------------- epilogue
+    const int et = threadIdx.x - 64;
+    const int ew = warp & 3;  // TMEM lane quarter
+    const uint32_t lane_off = static_cast<uint32_t>(ew * 32) << 16;
+    uint8_t* wbuf = base + C::kOutOff + (warp - 2) * 2 * kWarpOutBytes;
+    const uint32_t wbuf_s = sbase + C::kOutOff + (warp - 2) * 2 * kWarpOutBytes;
+    int wb = 0;
+    bool bye = false;  // arrived on the pair's final cluster barrier
+    // the four warps leave the tile loop together (named_all), so none is
+    // left alone at a named barrier
+    bool ok = dev::named_all(
+        1, 128, dev::mbar_wait(scale_bar, 0, abort_flag, p.dev_status, dev::kTimeoutEpilogue));
+    const float gs = *gscale_s;
+    for (int it = 0; it < my_tiles && ok; ++it) {
+      const int t = first + it * step;
+      const int tm = t % p.tiles_m, tn = t / p.tiles_m;
+      const int b = it % C::kAccBufs;
+      const uint32_t u = static_cast<uint32_t>(it / C::kAccBufs);
+      float* bs = bias_s + (it & 1) * kBN;
+#pragma unroll
+      for (int g = 0; g < kG; ++g) {
+        const int n = tn * kBN + g * kNvTile + et;
+        bs[g * kNvTile + et] = (p.bias && n < p.N) ? __ldg(p.bias + n) : 0.0f;
+      }
+      ok = dev::named_all(1, 128, dev::mbar_wait(tfull0 + 8 * b, u & 1, abort_flag, p.dev_status,
+                                                 dev::kTimeoutEpilogue));
+      if (!ok || it + 1 == my_tiles) {  // every MMA that reads the peer is done
+        dev::cluster_arrive_relaxed();
+        bye = true;
+      }
+      if (!ok) break;
+      dev::tc_fence_after();
+      const uint32_t tacc = tmem + lane_off + static_cast<uint32_t>(b) * C::kAccCols;
+      const int row0 = tm * 2 * kNvTile + px * kNvTile + ew * 32;
+#pragma unroll 1
+      for (int c = 0; c < kBN; c += 32) {
+        float v[32];
+        dev::tmem_ld32(tacc + c, v);
+        // accumulator read out: back to the MMA thread, if it will wait for it
+        if (c + 32 == kBN && it + C::kAccBufs < my_tiles) {
+          dev::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) dev::mbar_arrive_cluster(dev::map_to_rank(tempty0 + 8 * b, lead_rank));
+        }
+        const int n0 = tn * kBN + c;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = lin(v[j], gs, bs[c + j]);
+        if (n0 + 32 <= p.act_cols) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = gelu_tanh(v[j]);
+        } else if (n0 < p.act_cols) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const float gv = gelu_tanh(v[j]);
+            v[j] = n0 + j < p.act_cols ? gv : v[j];
+          }
+        }
+        if (n0 < p.N)
+          warp_store<false, 32>(v, wbuf + wb * kWarpOutBytes, wbuf_s + wb * kWarpOutBytes,
+                                &tmap_out, n0, row0, lane);
+        wb ^= 1;
+      }
+    }
+    if (!bye) dev::cluster_arrive_relaxed();
+    // the TMA stores have read their staging buffers before the CTA leaves
+    if (lane == 0) dev::bulk_wait_read<0>();
+  }
+  // neither CTA leaves (or frees TMEM) while the other may still take part
+  // in its MMAs or signal its barriers
+  dev::cluster_wait();
+  dev::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    dev::tc_fence_after();
+    dev::tmem_dealloc_pair(tmem, kNvTmemCols);
+  }
+}
+
+// Shared-memory attribute of a GEMM kernel, once per device.
+template <typename Kern>
+cudaError_t set_smem_once(Kern kern, int smem, std::mutex& mu, bool (&set)[64]) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(mu);
   if (!set[dev]) {
     const cudaError_t e =
-        cudaFuncSetAttribute(gemm_nvfp4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             NvCfg::kSmem);
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     set[dev] = true;
   }
@@ -552,7 +872,9 @@ cudaError_t prepare_nvfp4_gemm() {
 
 cudaError_t launch_nvfp4(const CUtensorMap& ta, const CUtensorMap& to, const NvGemmArgs& ga,
                          int sms, cudaStream_t stream) {
-  cudaError_t e = prepare_nvfp4_gemm();
+  static std::mutex mu;
+  static bool set[64] = {false};
+  cudaError_t e = set_smem_once(gemm_nvfp4_kernel, NvCfg::kSmem, mu, set);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(ga.num_tiles < sms ? ga.num_tiles : sms));
@@ -565,6 +887,59 @@ cudaError_t launch_nvfp4(const CUtensorMap& ta, const CUtensorMap& to, const NvG
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, gemm_nvfp4_kernel, ta, to, ga);
+}
+
+// ga.num_tiles counts 256-row pair tiles; at most one pair per two SMs and
+// no more pairs than can be resident at once (a persistent grid when there
+// are more tiles).
+template <int kBN>
+cudaError_t launch_nvfp4_pair(const CUtensorMap& ta, const CUtensorMap& tw,
+                              const CUtensorMap& tsa, const CUtensorMap& tsb,
+                              const CUtensorMap& to, const NvGemmArgs& ga, int sms,
+                              cudaStream_t stream) {
+  using C = NvPairCfg<kBN>;
+  auto kern = gemm_nvfp4_pair_kernel<kBN>;
+  static std::mutex mu;
+  static bool set[64] = {false};
+  static int capacity[64] = {0};
+  cudaError_t e = set_smem_once(kern, C::kSmem, mu, set);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(kNvThreads);
+  cfg.dynamicSmemBytes = C::kSmem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  int cap = 0;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (dev >= 0 && dev < 64 && capacity[dev] == 0) {
+      cfg.gridDim = dim3(2);
+      cfg.numAttrs = 1;
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n < 1) {
+        cudaGetLastError();
+        n = -1;  // unknown: one pair per two SMs
+      }
+      capacity[dev] = n;
+    }
+    cap = dev >= 0 && dev < 64 ? capacity[dev] : -1;
+  }
+  int pairs = sms / 2;
+  if (cap > 0 && cap < pairs) pairs = cap;
+  if (ga.num_tiles < pairs) pairs = ga.num_tiles;
+  if (pairs < 1) pairs = 1;
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs));
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kern, ta, tw, tsa, tsb, to, ga);
 }
 
 template <typename T>
@@ -710,8 +1085,51 @@ extern "C" frt_status frt_gemm_nvfp4(const uint8_t* a_q, int64_t lda, const uint
   ga.tiles_m = static_cast<int>(ceil_div(M, kNvTile));
   ga.dev_status = dev_status;
   const int sms = sm_count() > 0 ? sm_count() : 148;
-  ga.num_tiles = static_cast<int>(ga.tiles_m * ceil_div(N, kNvTile));
-  const cudaError_t e = launch_nvfp4(ta, to, ga, sms, as_cuda(stream));
+  cudaError_t e = cudaSuccess;
+  if (M <= kNvTile) {
+    ga.num_tiles = static_cast<int>(ga.tiles_m * ceil_div(N, kNvTile));
+    e = launch_nvfp4(ta, to, ga, sms, as_cuda(stream));
+  } else {
+    // 256-row tiles on CTA pairs.  The weight codes as packed k-tiles
+    // [tile][128 rows][128 bytes] (stored in their shared-memory image: no
+    // swizzle), one box = the half of a tile's channels that one CTA holds;
+    // the scales as lines of 256 bytes, one box = the four 512-byte atoms of
+    // a k-block (zero fill past the last 128-row group)
+    const int64_t nb_total = ceil_div(N, kNvTile);
+    ga.tiles_m = static_cast<int>(ceil_div(M, 2 * kNvTile));
+    CUtensorMap tw, tsa, tsb;
+    const cuuint64_t wdims[3] = {128u, static_cast<cuuint64_t>(kNvTile),
+                                 static_cast<cuuint64_t>(nb_total * ga.kb_total)};
+    const cuuint64_t wstr[2] = {128u, static_cast<cuuint64_t>(kNvOpBytes)};
+    // 256-channel tiles (one accumulator, twice the MACs per scale copy of
+    // A) when they still give every SM pair a tile; else 128-channel tiles
+    const bool wide = ga.tiles_m * ceil_div(N, 2 * kNvTile) >= sms / 2;
+    const int bn = wide ? 2 * kNvTile : kNvTile;
+    const cuuint32_t wbox[3] = {128u, static_cast<cuuint32_t>(bn / 2), 1u};
+    const cuuint32_t estr3[3] = {1, 1, 1};
+    const cuuint64_t adims[2] = {256u,
+                                 static_cast<cuuint64_t>(ceil_div(M, kNvTile) * ga.kc_total * 2)};
+    const cuuint64_t bdims[2] = {256u, static_cast<cuuint64_t>(nb_total * ga.kc_total * 2)};
+    const cuuint64_t sstr[1] = {256u};
+    const cuuint32_t sbox[2] = {256u, 8u};
+    const cuuint32_t estr2[2] = {1, 1};
+    if (encode(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(w_packed), wdims, wstr,
+               wbox, estr3, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS ||
+        encode(&tsa, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(a_sf), adims, sstr,
+               sbox, estr2, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS ||
+        encode(&tsb, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(w_sf), bdims, sstr,
+               sbox, estr2, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return FRT_ERR_CUDA;
+    ga.num_tiles = static_cast<int>(ga.tiles_m * ceil_div(N, bn));
+    e = wide ? launch_nvfp4_pair<2 * kNvTile>(ta, tw, tsa, tsb, to, ga, sms, as_cuda(stream))
+             : launch_nvfp4_pair<kNvTile>(ta, tw, tsa, tsb, to, ga, sms, as_cuda(stream));
+  }
   if (e != cudaSuccess) {
     cudaGetLastError();
     return FRT_ERR_CUDA;

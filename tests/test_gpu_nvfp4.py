@@ -94,6 +94,7 @@ def _gemm_case(M, N, K, act_cols, bias=True, seed=0, cols=None):
     (300, 272, 1024, 0, True),     # N tail inside a 128-channel tile
     (768, 2560, 2048, 0, True),    # the encoder's QKV shape
     (256, 19456, 256, 9000, True), # more tiles than SMs, the GELU boundary inside a tile
+    (300, 25744, 256, 12000, True),  # 256-channel pair tiles with row and channel tails
 ])
 def test_gemm(M, N, K, act_cols, bias):
     y, ref, sumabs = _gemm_case(M, N, K, act_cols, bias, seed=M + N + K)
