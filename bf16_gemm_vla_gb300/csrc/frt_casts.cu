@@ -374,12 +374,13 @@ __device__ __forceinline__ void encode16(const uint4& w, float sc, float r, bool
 #pragma unroll
       for (int k = 0; k < 4; ++k) hi |= quantize_one<true>(f[4 + k], sc, r, fast_ok) << (8 * k);
     }
+  } else if constexpr (sizeof(T) == 2) {
+    const uint2 w2 = encode8_ocp(f, sc, r, fast_ok);
+    lo = w2.x;
+    hi = w2.y;
   } else {
     lo = canonical_nan_x4(quantize_pair_ocp(f[0], f[1], sc, r, fast_ok) |
                           (quantize_pair_ocp(f[2], f[3], sc, r, fast_ok) << 16));
-    if constexpr (sizeof(T) == 2)
-      hi = canonical_nan_x4(quantize_pair_ocp(f[4], f[5], sc, r, fast_ok) |
-                            (quantize_pair_ocp(f[6], f[7], sc, r, fast_ok) << 16));
   }
   if constexpr (sizeof(T) == 2)
     *reinterpret_cast<uint2*>(dst) = make_uint2(lo, hi);

@@ -1,6 +1,7 @@
 """Runs one layer of the path a few times, for profiling (e.g. under ncu).
 
     python -m bf16_gemm_vla_gb300.run_case --kind fp8 --M 50 --K 1024 --N 4096 --reps 3
+    python -m bf16_gemm_vla_gb300.run_case --kind nvfp4 --M 768 --K 2048 --N 16384 --reps 3
     python -m bf16_gemm_vla_gb300.run_case --op quantize --M 768 --K 16384 --reps 3
 
 Synthetic inputs are drawn on the device (seeded): activations N(0,1) bf16,
@@ -19,7 +20,7 @@ from . import frt, layers
 
 def main(argv=None):
     ap = argparse.ArgumentParser()
-    ap.add_argument("--kind", choices=("fp8", "bf16"), default="fp8")
+    ap.add_argument("--kind", choices=("fp8", "bf16", "nvfp4"), default="fp8")
     ap.add_argument("--M", type=int, default=50)
     ap.add_argument("--K", type=int, default=1024)
     ap.add_argument("--N", type=int, default=4096)
@@ -38,6 +39,8 @@ def main(argv=None):
     x = torch.randn((a.M, a.K), generator=g, device=dev).to(torch.bfloat16)
     w = torch.randn((a.K, a.N), generator=g, device=dev) * 0.02
     b = torch.randn((a.N,), generator=g, device=dev) * 0.1
+    if a.kind == "nvfp4":
+        return nvfp4_case(a, x, w, b)
     pw = layers.prepare_fp8(w, b) if a.kind == "fp8" else layers.prepare_bf16(w, b)
     lin = layers.Linear(pw, a.M, act_cols=a.act_cols)
     if a.kind == "fp8":
@@ -67,6 +70,30 @@ def main(argv=None):
                                                           e0.elapsed_time(e1) * 1e3 / a.reps))
 
 
+def _time(a, once, what):
+    once()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(a.reps):
+        once()
+    e1.record()
+    torch.cuda.synchronize()
+    frt.check_device_status()
+    if not a.quiet:
+        print("%s: %.2f us per launch" % (what, e0.elapsed_time(e1) * 1e3 / a.reps))
+
+
+def nvfp4_case(a, x, w, b):
+    pw = layers.prepare_nvfp4(w, b)
+    qa, sfa, ga = frt.frt_quantize_nvfp4(x)
+    out = torch.empty((a.M, a.N), dtype=torch.bfloat16, device=x.device)
+    _time(a, lambda: frt.frt_gemm_nvfp4(qa, sfa, ga, pw.packed, pw.sf, pw.g, a.N, bias=pw.bias,
+                                        act_cols=a.act_cols, out=out),
+          "nvfp4 M=%d K=%d N=%d" % (a.M, a.K, a.N))
+
+
 def quantize_case(a, dev):
     g = torch.Generator(device=dev)
     g.manual_seed(0)
@@ -74,10 +101,11 @@ def quantize_case(a, dev):
     q = torch.empty((a.M, a.K), dtype=torch.uint8, device=dev)
     s = torch.empty((1,), dtype=torch.float32, device=dev)
     ws = torch.zeros((4096,), dtype=torch.float32, device=dev)  # header zero-filled once
-    one = torch.ones((1,), dtype=torch.float32, device=dev)
+    cal = torch.empty((1,), dtype=torch.float32, device=dev)
+    frt.frt_quantize_e4m3(x, q=q, scale=cal, workspace=ws)  # the calibrated static scale
 
     def once():
-        frt.frt_quantize_e4m3(x, static_scale=one if a.static_scale else None, q=q, scale=s,
+        frt.frt_quantize_e4m3(x, static_scale=cal if a.static_scale else None, q=q, scale=s,
                               workspace=ws)
 
     once()
