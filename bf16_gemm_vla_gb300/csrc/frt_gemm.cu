@@ -29,7 +29,8 @@
 // or by TMA over the packed buffer (pairs).  Warp roles: warp 0 issues the
 // copies, one thread of warp 1 issues tcgen05.mma into TMEM, warps 2-5 run
 // the epilogue (large M: bf16 staged in swizzled shared memory and written
-// by TMA tensor stores; small M: stored straight from registers).
+// by TMA tensor stores; small M: each warp's rows staged in shared memory and
+// written by 16-byte stores).
 //
 // Scheduling:
 //   * without split-K the grid is persistent (one CTA, or pair, per SM walks
@@ -77,6 +78,7 @@ constexpr int kWTile = kTile * kKBytes;  // bytes of one packed weight tile
 constexpr int kSmemMax = 232448;         // dynamic shared memory limit per CTA
 constexpr int kPairMinSmem = 200 * 1024;  // shared memory floor of a pair CTA
 constexpr int kOutBytes = 4 * 2 * kWarpOutBytes;  // 4 epilogue warps x 2 buffers
+constexpr int kSwapStoreBytes = 32 * 64;          // small M: a warp's staged bf16 rows
 constexpr int kBarRegion = 512;          // mbarriers, TMEM address, abort flag
 constexpr int kMaxSplits = 8;            // portable cluster size
 constexpr int kMaxStages = 8;
@@ -109,7 +111,7 @@ struct GemmArgs {
   int recv_off;
   int tail_off;        // per-channel scale/bias, then mbarriers
   int split_global;    // split-K partials exchanged through the workspace (pairs)
-  __nv_bfloat16* out;  // small M: output rows stored straight from registers
+  __nv_bfloat16* out;  // small M: output rows written by the epilogue warps
   int ldo;
   float* ws_part;      // split_global: partial chunks, one slot per (tile, CTA, chunk, split)
   unsigned* ws_flag;   // split_global: per (tile, CTA, owner split) arrival counters
@@ -144,17 +146,29 @@ struct Cfg {
   static_assert(!(kSwap && kPair), "CTA pairs take large-M tiles");
 };
 
-// Small M: stores kRows output rows of one channel straight from registers
-// (v[j] = row y0 + j; the lanes of a warp hold consecutive channels, so each
-// row's store instruction covers 64 contiguous bytes).  Rows >= M and
-// channels >= N are not written.
+// Small M: one warp's output rows.  Lane l holds channel n0 + l (n0 a
+// multiple of 32) of rows y0 .. y0 + kRows - 1 (v[j] = row y0 + j).  The
+// warp's kRows x 32 bf16 values are staged in `sb` (kRows x 64 bytes of
+// this warp's shared memory) and written with one 16-byte store per lane and
+// 8 rows (N and ldo are multiples of 8 and the output is 16-byte aligned, so
+// a group of 8 channels is either whole or past N).  Rows >= M and channels
+// >= N are not written.
 template <int kRows>
-__device__ __forceinline__ void store_rows(const float* v, const GemmArgs& p, int y0, int n) {
-  if (n >= p.N) return;
-  __nv_bfloat16* dst = p.out + static_cast<size_t>(y0) * p.ldo + n;
+__device__ __forceinline__ void store_rows(const float* v, const GemmArgs& p, int y0, int n0,
+                                           int lane, __nv_bfloat16* sb) {
+  __syncwarp();  // the previous chunk's reads of sb are done
 #pragma unroll
-  for (int j = 0; j < kRows; ++j)
-    if (y0 + j < p.M) dst[static_cast<size_t>(j) * p.ldo] = __float2bfloat16_rn(v[j]);
+  for (int j = 0; j < kRows; ++j) sb[j * 32 + lane] = __float2bfloat16_rn(v[j]);
+  __syncwarp();
+  const int seg = lane & 3;
+  const int n = n0 + seg * 8;
+#pragma unroll
+  for (int r0 = 0; r0 < kRows; r0 += 8) {
+    const int r = r0 + (lane >> 2);
+    const uint4 w = *reinterpret_cast<const uint4*>(sb + r * 32 + seg * 8);
+    if (y0 + r < p.M && n < p.N)
+      *reinterpret_cast<uint4*>(p.out + static_cast<size_t>(y0 + r) * p.ldo + n) = w;
+  }
 }
 
 // Byte offset of float4 granule q of row r in a split-K partial chunk of
@@ -625,6 +639,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row = ew * 32 + lane;   // TMEM lane = tile row
     const uint32_t lane_off = static_cast<uint32_t>(ew * 32) << 16;
     uint8_t* wbuf = base + p.outbuf_off + (warp - 2) * 2 * kWarpOutBytes;  // this warp's 2 buffers
+    // small M: this warp's row-store staging (32 rows x 64 bytes), after the
+    // GeGLU's lane-exchange buffers if there are any
+    __nv_bfloat16* swap_sb = reinterpret_cast<__nv_bfloat16*>(
+        base + p.outbuf_off + (p.geglu ? kOutBytes : 0) + (warp - 2) * kSwapStoreBytes);
     const uint32_t wbuf_s = sbase + p.outbuf_off + (warp - 2) * 2 * kWarpOutBytes;
     int wb = 0;
     bool ok = true;
@@ -758,10 +776,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (!p.geglu) {
             if (p.s_cols) amax_col<32>(p, amax, v, rows_of_tile_m0 + c32, tn * kTile + row);
-            store_rows<32>(v, p, rows_of_tile_m0 + c32, tn * kTile + row);
+            store_rows<32>(v, p, rows_of_tile_m0 + c32, tn * kTile + ew * 32, lane, swap_sb);
           } else if (geglu_rows(v, 32, wb)) {
             if (p.s_cols) amax_col<32>(p, amax, v, rows_of_tile_m0 + c32, tn * 64 + row);
-            store_rows<32>(v, p, rows_of_tile_m0 + c32, tn * 64 + row);
+            store_rows<32>(v, p, rows_of_tile_m0 + c32, tn * 64 + ew * 32, lane, swap_sb);
           }
         }
         wb ^= 1;
@@ -1017,24 +1035,33 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int lc = 0; lc < owned; ++lc) {
             float own[8];
             dev::tmem_ld8(tacc + (own_c0 + lc) * 8, own);
-            // the S partials in rank order, this CTA's own at its rank; the
-            // receive slots hold the other ranks in rank order
+            // the other ranks' partials (receive slot q holds rank q below
+            // this CTA's rank, q + 1 from it on), loaded three slots ahead of
+            // their additions
+            float4 px[3][2];
+            auto load_slot = [&](int q, float4 (&x)[2]) {
+              const uint8_t* src = recv + (q * owned_max + lc) * chunk_bytes;
+              x[0] = *reinterpret_cast<const float4*>(src + chunk_off(row, 0, 8));
+              x[1] = *reinterpret_cast<const float4*>(src + chunk_off(row, 1, 8));
+            };
+#pragma unroll
+            for (int q = 0; q < 3; ++q)
+              if (q < S - 1) load_slot(q, px[q]);
+            // the S partials added in rank order, this CTA's own at its rank
             float sum[8];
 #pragma unroll
             for (int j = 0; j < 8; ++j) sum[j] = 0.0f;
 #pragma unroll
-            for (int r = 0; r < kMaxSplits; ++r) {
-              if (r >= S) break;
-              if (r == rank) {
+            for (int q = 0; q < kMaxSplits; ++q) {
+              if (q == rank) {
 #pragma unroll
                 for (int j = 0; j < 8; ++j) sum[j] += own[j];
-              } else {
-                const uint8_t* src =
-                    recv + ((r < rank ? r : r - 1) * owned_max + lc) * chunk_bytes;
-                const float4 x0 = *reinterpret_cast<const float4*>(src + chunk_off(row, 0, 8));
-                const float4 x1 = *reinterpret_cast<const float4*>(src + chunk_off(row, 1, 8));
-                sum[0] += x0.x; sum[1] += x0.y; sum[2] += x0.z; sum[3] += x0.w;
-                sum[4] += x1.x; sum[5] += x1.y; sum[6] += x1.z; sum[7] += x1.w;
+              }
+              if (q < kMaxSplits - 1 && q < S - 1) {
+                const float4(&x)[2] = px[q % 3];
+                sum[0] += x[0].x; sum[1] += x[0].y; sum[2] += x[0].z; sum[3] += x[0].w;
+                sum[4] += x[1].x; sum[5] += x[1].y; sum[6] += x[1].z; sum[7] += x[1].w;
+                if (q + 3 < kMaxSplits - 1 && q + 3 < S - 1) load_slot(q + 3, px[q % 3]);
               }
             }
 #pragma unroll
@@ -1045,10 +1072,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (!p.geglu) {
               if (p.s_cols) amax_col<8>(p, amax, sum, tm * kBN + (own_c0 + lc) * 8, tn * kTile + row);
-              store_rows<8>(sum, p, tm * kBN + (own_c0 + lc) * 8, tn * kTile + row);
-            } else if (geglu_rows(sum, 8, lc & 1)) {
+              store_rows<8>(sum, p, tm * kBN + (own_c0 + lc) * 8, tn * kTile + ew * 32, lane,
+                            swap_sb);
+            } else if (geglu_rows(sum, 8, lc & 1)) {  // the gate lanes: warps 0-1 of 4
               if (p.s_cols) amax_col<8>(p, amax, sum, tm * kBN + (own_c0 + lc) * 8, tn * 64 + row);
-              store_rows<8>(sum, p, tm * kBN + (own_c0 + lc) * 8, tn * 64 + row);
+              store_rows<8>(sum, p, tm * kBN + (own_c0 + lc) * 8, tn * 64 + ew * 32, lane,
+                            swap_sb);
             }
           }
         } else {
@@ -1155,9 +1184,10 @@ bool layout(Plan& pl, int stage_bytes, int cap = kSmemMax) {
   const int pipe = pl.stages * stage_bytes;
   pl.outbuf_off = pipe;
   pl.recv_off = 0;
-  // small M stores from registers (a GeGLU exchanges its up values through
-  // the same 16 KiB)
-  int tail = pipe + (pl.swap && !pl.geglu ? 0 : kOutBytes);
+  // small M stages each warp's rows (2 KiB a warp) for 16-byte stores, after
+  // the 16 KiB through which a GeGLU exchanges its up values (the large-M
+  // output buffers)
+  int tail = pipe + (pl.swap ? (pl.geglu ? kOutBytes : 0) + 4 * kSwapStoreBytes : kOutBytes);
   if (pl.splits > 1 && !pl.split_global) {
     const int nchunks = pl.bn / pl.chunk_cols;
     const int chunk = kTile * pl.chunk_cols * 4;
