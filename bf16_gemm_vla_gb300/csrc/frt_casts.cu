@@ -324,13 +324,17 @@ __global__ void __launch_bounds__(kQThreads) encode_tensor_kernel(
 // s = amax / max (1 if amax is 0); finally every CTA encodes its part from
 // chip.  x is read from memory once.
 //
-// The barrier is sense-reversing: each CTA reads the generation (after the
-// previous grid has completed), folds its maximum into the header's running
-// maximum (an integer atomic max on the fp32 bits, which orders non-negative
-// floats as their values) and arrives on the arrival count
-// (acquire-release); the last arrival reads the maximum, turns it into s,
-// resets the maximum and the count and publishes the next generation
-// together with s in one 64-bit store, which the others poll.
+// The barrier: each CTA reads the generation (after the previous grid has
+// completed), folds its maximum into this call's running-maximum word (an
+// integer atomic max on the fp32 bits, which orders non-negative floats as
+// their values; the two words alternate between calls by the generation's
+// parity) and arrives on the arrival count (acquire-release, so the count's
+// read-modify-writes carry every CTA's maximum).  A CTA that sees the count
+// complete (acquire) reads the maximum itself and turns it into s = amax /
+// max (1 if amax is 0).  The last arrival does the same, then clears the
+// other parity's maximum and the count for the next call and publishes the
+// next generation together with s in one 64-bit store, which a CTA that
+// missed the complete count (already cleared) takes s from.
 // Waits are bounded; a CTA that gives up records a code in the header's
 // status word and uses s = NaN, so the result is visibly invalid.
 constexpr int kResThreads = 1024;   // shared-memory path
@@ -341,7 +345,8 @@ constexpr int kResSmem = kResChunk * kResMaxChunks;
 constexpr int kRegVecs = 3;         // register path: 16-byte vectors per thread
 constexpr int kHeaderFloats = 64;   // workspace header: 256 bytes
 // header words: [0] arrivals, [1] status, [2] generation and [3] scale bits
-// (one 64-bit word), [4] running max |x| (fp32 bits)
+// (one 64-bit word), [4] and [5] running max |x| (fp32 bits) of the calls
+// with an even and an odd generation
 
 template <typename T>
 __device__ __forceinline__ int unpack16(const uint4& w, float (&f)[8]) {
@@ -423,24 +428,36 @@ __device__ __forceinline__ float grid_scale(float m, unsigned g0, unsigned* hdr,
   if (threadIdx.x == 0) {
     bool fail = failed;
     float sc;
+    auto scale_of = [](unsigned amax_bits) {
+      const float a = __uint_as_float(amax_bits);
+      return a == 0.0f ? 1.0f : __fdiv_rn(a, kFnuz ? 240.0f : 448.0f);
+    };
+    unsigned* run_max = hdr + 4 + (g0 & 1u);  // this call's; cleared by the previous one
     // m >= 0 and never NaN (fmaxf from 0): its bits order as its value.  The
     // max is ordered before the arrival by the arrival's release.
-    atomicMax(hdr + 4, __float_as_uint(m));
-    if (atom_add_acq_rel_gpu(hdr, 1u) == gridDim.x - 1) {
+    atomicMax(run_max, __float_as_uint(m));
+    const unsigned grid = gridDim.x;
+    if (atom_add_acq_rel_gpu(hdr, 1u) == grid - 1) {
       // every other CTA's max was released before its arrival, and this
       // arrival's acquire orders the load after them
-      const float a = __uint_as_float(ld_relaxed_gpu(hdr + 4));
-      sc = a == 0.0f ? 1.0f : __fdiv_rn(a, kFnuz ? 240.0f : 448.0f);
+      sc = scale_of(ld_relaxed_gpu(run_max));
       // the resets reach memory before the next grid starts (grid
-      // completion); the waiters read nothing but the published word, so
-      // none of these stores needs ordering
-      hdr[4] = 0u;
+      // completion); a waiter that reads the cleared count takes s from
+      // the published word instead
+      hdr[4 + ((g0 + 1u) & 1u)] = 0u;
       hdr[0] = 0u;
       st_relaxed_gpu_u64(hdr + 2, static_cast<unsigned long long>(g0 + 1u) |
                                       (static_cast<unsigned long long>(__float_as_uint(sc)) << 32));
     } else {
       const uint64_t t0 = dev::globaltimer_ns();
       for (uint32_t it = 0;; ++it) {
+        // the complete count (its acquire reads the last of the arrivals'
+        // read-modify-writes, after which every max is visible) ...
+        if (ld_acquire_gpu(hdr) == grid) {
+          sc = scale_of(ld_relaxed_gpu(run_max));
+          break;
+        }
+        // ... or, once the last arrival has cleared it, the published s
         const unsigned long long w = ld_relaxed_gpu_u64(hdr + 2);
         if (static_cast<unsigned>(w) != g0) {
           sc = __uint_as_float(static_cast<unsigned>(w >> 32));
