@@ -367,8 +367,10 @@ def kernel_durations(sets, iters):
 def back_to_back_durations(sets, reps):
     """Per-layer device durations of the quantize (amax + encode) and of the
     GEMM in steady state: each is the mean over launches of that one kernel
-    back to back on the rotating sets (inputs larger than L2), captured in
-    one CUDA graph and timed with events around the replays."""
+    back to back on rotating inputs larger than 4x L2 (the GEMM over the
+    sets' weights and activations, the quantize over the sets' activations
+    and copies of them), captured in one CUDA graph and timed with events
+    around the replays."""
     from bf16_gemm_vla_gb300 import frt
 
     # each graph cycles the sets `cycles` times (at least 32 launches), so the
@@ -383,19 +385,29 @@ def back_to_back_durations(sets, reps):
                     frt.frt_gemm_fp8(lin.q, lin.a_scale, lin.w.packed, lin.w.w_scale, lin.w.N,
                                      bias=lin.w.bias, out=lin.out, workspace=lin.gws)
 
-        def run_quants(li=li):
-            for _ in range(cycles):
-                for st in sets:
-                    lin, x = st.layers[li], st.inputs[li]
+        # the quantize reads only the activations: copies of them so that its
+        # rotation too is larger than 4x L2
+        xs = [st.inputs[li] for st in sets]
+        per_x = xs[0].numel() * xs[0].element_size()
+        extra = max(0, -(-4 * l2_bytes() // per_x) - len(xs))
+        xs = xs + [xs[i % len(sets)].clone() for i in range(extra)]
+        qcycles = max(1, -(-32 // len(xs)))
+
+        def run_quants(li=li, xs=xs):
+            for _ in range(qcycles):
+                for i, x in enumerate(xs):
+                    lin = sets[i % len(sets)].layers[li]
                     frt.frt_quantize_e4m3(x, frt.PER_TENSOR, frt.OCP, q=lin.q, scale=lin.a_scale,
                                           workspace=lin.ws)
 
-        for fn, dst in ((run_quants, quant), (run_gemms, gemm)):
+        for fn, dst, n in ((run_quants, quant, qcycles * len(xs)),
+                           (run_gemms, gemm, cycles * len(sets))):
             g = capture(fn)
             g.replay()
             secs = device_time(lambda i: g.replay(), reps)
-            dst.append(secs / (reps * cycles * len(sets)))
+            dst.append(secs / (reps * n))
             del g
+        del xs
     return quant, gemm
 
 
@@ -723,15 +735,20 @@ def run_components(args, device, sampler, peaks):
     frt.check_device_status()
     qus = []
     for li in range(len(set0.layers)):
-        def qrun(li=li):
-            for st_ in sets:
-                lin = st_.layers[li]
-                frt.frt_quantize_e4m3(st_.inputs[li], frt.PER_TENSOR, frt.OCP,
+        # the sets' activations and copies of them: more than 4x L2
+        xs = [st_.inputs[li] for st_ in sets]
+        per_x = xs[0].numel() * xs[0].element_size()
+        xs = xs + [xs[i % R].clone() for i in range(max(0, -(-4 * l2_bytes() // per_x) - R))]
+
+        def qrun(li=li, xs=xs):
+            for i, x in enumerate(xs):
+                lin = sets[i % R].layers[li]
+                frt.frt_quantize_e4m3(x, frt.PER_TENSOR, frt.OCP,
                                       static_scale=lin.a_scale, q=lin.q, scale=lin.s_out)
         g = capture(qrun)
         g.replay()
-        qus.append(device_time(lambda i: g.replay(), 20) / (20 * R) * 1e6)
-        del g
+        qus.append(device_time(lambda i: g.replay(), 20) / (20 * len(xs)) * 1e6)
+        del g, xs
     out["encoder_m768_fp8_static_scale"] = {
         "tflops": set0.flops() / secs / 1e12, "ms_per_step": secs * 1e3,
         "launches_per_step": launches_of(set0.forward), "scales": scales[0],
