@@ -83,6 +83,19 @@ __device__ __forceinline__ uint32_t e2m1_code_div(float x, float e, float r, boo
   return e2m1_code(__fdiv_rn(x, e));
 }
 
+// E2M1 codes of the two fp32 lanes of v by the hardware conversion (round to
+// nearest even, saturating at +-6, the sign of a zero kept): the low lane in
+// the low nibble of the byte returned.  Not for NaN (E2M1 has no NaN code).
+__device__ __forceinline__ uint32_t cvt_e2m1x2(unsigned long long v) {
+  float lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+  uint32_t r;
+  asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u32.u8 %0, t;\n\t}"
+      : "=r"(r)
+      : "f"(hi), "f"(lo));
+  return r;
+}
+
 // Value of a non-negative OCP E4M3 byte (no NaN: the block scales saturate).
 __device__ __forceinline__ float e4m3_value_pos(uint32_t b) {
   const uint32_t e = (b >> 3) & 15u, m = b & 7u;
@@ -194,8 +207,69 @@ __global__ void __launch_bounds__(kNvQThreads) nvfp4_encode_kernel(
   const uint32_t vpad = static_cast<uint32_t>((V + 127) / 128 * 128);
   const int64_t kc_total = Kd / 64;
   const uint32_t total = vpad * nb;
-  for (uint32_t t = blockIdx.x * kNvQThreads + threadIdx.x; t < total;
-       t += gridDim.x * kNvQThreads) {
+  const uint32_t stride = gridDim.x * kNvQThreads;
+  // block (v, j): vector v (a row of x, or a column when kAlongRows), its
+  // elements 16 j ... 16 j + 15 in f; writes the codes and the block scale
+  auto encode_block = [&](const float (&f)[kBlk], int64_t v, int64_t j) {
+    float b = 0.0f;
+    bool nan = false;
+#pragma unroll
+    for (int i = 0; i < kBlk; ++i) {
+      b = fmaxf(b, fabsf(f[i]));
+      nan |= f[i] != f[i];
+    }
+    const uint32_t sbyte = encode_e4m3<false>(__fdiv_rn(b, d));  // b >= 0, d > 0: non-negative
+    const float e = __fmul_rn(e4m3_value_pos(sbyte), g);
+    const float r = __frcp_rn(e);
+    const bool fast = e > 0.0f && (__float_as_uint(r) >> 23) - 1u < 254u;
+    // the 16 codes as 8 bytes, element 2 p in the low nibble of byte p (lo:
+    // bytes 0-3, hi: bytes 4-7).  Fast path: the bracket of e2m1_code_div
+    // on packed products, both ends converted by the hardware, one test for
+    // the block; a block with a NaN, a bracket that straddles a rounding
+    // boundary or no usable reciprocal takes the element-wise path.
+    uint32_t lo = 0u, hi = 0u;
+    bool done = false;
+    if (fast && !nan) {
+      const unsigned long long rr = f32x2(r, r);
+      const unsigned long long dn = f32x2(1.0f - 0x1p-20f, 1.0f - 0x1p-20f);
+      const unsigned long long up = f32x2(1.0f + 0x1p-20f, 1.0f + 0x1p-20f);
+      uint32_t lo_u = 0u, hi_u = 0u;
+#pragma unroll
+      for (int p2 = 0; p2 < kBlk / 2; ++p2) {
+        const unsigned long long y = mul_f32x2(f32x2(f[2 * p2], f[2 * p2 + 1]), rr);
+        const uint32_t cd = cvt_e2m1x2(mul_f32x2(y, dn));
+        const uint32_t cu = cvt_e2m1x2(mul_f32x2(y, up));
+        if (p2 < 4) {
+          lo |= cd << (8 * p2);
+          lo_u |= cu << (8 * p2);
+        } else {
+          hi |= cd << (8 * (p2 - 4));
+          hi_u |= cu << (8 * (p2 - 4));
+        }
+      }
+      done = lo == lo_u && hi == hi_u;
+    }
+    if (!done) {
+      lo = 0u;
+      hi = 0u;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        lo |= (e > 0.0f ? e2m1_code_div(f[i], e, r, fast) : 0u) << (4 * i);
+        hi |= (e > 0.0f ? e2m1_code_div(f[8 + i], e, r, fast) : 0u) << (4 * i);
+      }
+    }
+    if constexpr (kAlongRows) {
+      // [K/2 x V]: byte (8 j + p, v) holds elements 16 j + 2 p (low) and + 1
+#pragma unroll
+      for (int p2 = 0; p2 < kBlk / 2; ++p2)
+        q[(j * (kBlk / 2) + p2) * V + v] =
+            static_cast<uint8_t>(((p2 < 4 ? lo : hi) >> (8 * (p2 & 3))) & 0xFFu);
+    } else {
+      *reinterpret_cast<uint2*>(q + v * (Kd / 2) + j * (kBlk / 2)) = make_uint2(lo, hi);
+    }
+    sf[sf_offset(v, j, kc_total)] = static_cast<uint8_t>(sbyte);
+  };
+  for (uint32_t t = blockIdx.x * kNvQThreads + threadIdx.x; t < total; t += stride) {
     int64_t v, j;
     if constexpr (kAlongRows) {  // consecutive threads: consecutive columns (coalesced)
       v = t % vpad;
@@ -204,55 +278,32 @@ __global__ void __launch_bounds__(kNvQThreads) nvfp4_encode_kernel(
       v = t / nb;
       j = t % nb;
     }
-    uint32_t sbyte = 0u;
-    if (v < V) {
-      float f[kBlk];
-      if constexpr (kAlongRows) {
+    if (v >= V) {
+      sf[sf_offset(v, j, kc_total)] = 0u;  // padding vectors: scale 0
+      continue;
+    }
+    float f[kBlk];
+    if constexpr (kAlongRows) {
 #pragma unroll
-        for (int i = 0; i < kBlk; ++i) f[i] = nv_to_f32<T>(x[(j * kBlk + i) * ldx + v]);
-      } else if constexpr (sizeof(T) == 2) {
-        const uint4* src = reinterpret_cast<const uint4*>(x + v * ldx + j * kBlk);
-        const uint4 w0 = src[0], w1 = src[1];
-        const uint32_t ws8[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+      for (int i = 0; i < kBlk; ++i) f[i] = nv_to_f32<T>(x[(j * kBlk + i) * ldx + v]);
+    } else if constexpr (sizeof(T) == 2) {
+      const uint4* src = reinterpret_cast<const uint4*>(x + v * ldx + j * kBlk);
+      const uint4 w0 = src[0], w1 = src[1];
+      const uint32_t ws8[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          f[2 * k] = __uint_as_float(ws8[k] << 16);
-          f[2 * k + 1] = __uint_as_float(ws8[k] & 0xFFFF0000u);
-        }
-      } else {
-        const float4* src = reinterpret_cast<const float4*>(x + v * ldx + j * kBlk);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const float4 a = src[k];
-          f[4 * k] = a.x; f[4 * k + 1] = a.y; f[4 * k + 2] = a.z; f[4 * k + 3] = a.w;
-        }
+      for (int k = 0; k < 8; ++k) {
+        f[2 * k] = __uint_as_float(ws8[k] << 16);
+        f[2 * k + 1] = __uint_as_float(ws8[k] & 0xFFFF0000u);
       }
-      float b = 0.0f;
+    } else {
+      const float4* src = reinterpret_cast<const float4*>(x + v * ldx + j * kBlk);
 #pragma unroll
-      for (int i = 0; i < kBlk; ++i) b = fmaxf(b, fabsf(f[i]));
-      sbyte = encode_e4m3<false>(__fdiv_rn(b, d));  // b >= 0, d > 0: a non-negative byte
-      const float e = __fmul_rn(e4m3_value_pos(sbyte), g);
-      const float r = __frcp_rn(e);
-      const bool fast = e > 0.0f && (__float_as_uint(r) >> 23) - 1u < 254u;
-      uint32_t c[kBlk];
-#pragma unroll
-      for (int i = 0; i < kBlk; ++i) c[i] = e > 0.0f ? e2m1_code_div(f[i], e, r, fast) : 0u;
-      if constexpr (kAlongRows) {
-        // [K/2 x V]: byte (8 j + p, v) holds elements 16 j + 2 p (low) and + 1
-#pragma unroll
-        for (int p2 = 0; p2 < kBlk / 2; ++p2)
-          q[(j * (kBlk / 2) + p2) * V + v] = static_cast<uint8_t>(c[2 * p2] | (c[2 * p2 + 1] << 4));
-      } else {
-        uint32_t lo = 0u, hi = 0u;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          lo |= c[i] << (4 * i);
-          hi |= c[8 + i] << (4 * i);
-        }
-        *reinterpret_cast<uint2*>(q + v * (Kd / 2) + j * (kBlk / 2)) = make_uint2(lo, hi);
+      for (int k = 0; k < 4; ++k) {
+        const float4 a = src[k];
+        f[4 * k] = a.x; f[4 * k + 1] = a.y; f[4 * k + 2] = a.z; f[4 * k + 3] = a.w;
       }
     }
-    sf[sf_offset(v, j, kc_total)] = static_cast<uint8_t>(sbyte);
+    encode_block(f, v, j);
   }
   // the amax word is read by every CTA before it counts itself done here; the
   // last one clears it (and the count) for the next call

@@ -3,6 +3,7 @@
     python -m bf16_gemm_vla_gb300.run_case --kind fp8 --M 50 --K 1024 --N 4096 --reps 3
     python -m bf16_gemm_vla_gb300.run_case --kind nvfp4 --M 768 --K 2048 --N 16384 --reps 3
     python -m bf16_gemm_vla_gb300.run_case --op quantize --M 768 --K 16384 --reps 3
+    python -m bf16_gemm_vla_gb300.run_case --op nvfp4_quantize --M 768 --K 16384 --reps 3
 
 Synthetic inputs are drawn on the device (seeded): activations N(0,1) bf16,
 weights N(0,0.02), bias N(0,0.1).  The FP8 path quantizes the activations
@@ -28,12 +29,20 @@ def main(argv=None):
     ap.add_argument("--reps", type=int, default=3)
     ap.add_argument("--with-quantize", action="store_true")
     ap.add_argument("--quiet", action="store_true")
-    ap.add_argument("--op", choices=("gemm", "quantize"), default="gemm")
+    ap.add_argument("--op", choices=("gemm", "quantize", "nvfp4_quantize"), default="gemm")
     ap.add_argument("--static-scale", action="store_true")
     a = ap.parse_args(argv)
     dev = torch.device("cuda")
     if a.op == "quantize":
         return quantize_case(a, dev)
+    if a.op == "nvfp4_quantize":
+        g = torch.Generator(device=dev)
+        g.manual_seed(0)
+        x = torch.randn((a.M, a.K), generator=g, device=dev).to(torch.bfloat16)
+        q, sf, s = frt.frt_quantize_nvfp4(x)
+        ws = frt.nvfp4_workspace(dev)
+        return _time(a, lambda: frt.frt_quantize_nvfp4(x, q=q, sf=sf, scale=s, workspace=ws),
+                     "nvfp4 quantize %d x %d" % (a.M, a.K))
     g = torch.Generator(device=dev)
     g.manual_seed(0)
     x = torch.randn((a.M, a.K), generator=g, device=dev).to(torch.bfloat16)
