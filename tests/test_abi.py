@@ -153,3 +153,91 @@ def test_decoder_boundary_rejects_bad_arguments(lib):
         a = list(ok)
         a[i] = v
         assert f(*a) == code[want], (i, v)
+
+
+def test_nvfp4_sizes(lib):
+    # one E4M3 block scale per 16 elements of K, vectors padded to 128
+    assert lib.frt_nvfp4_scale_bytes(768, 2048) == 768 * 2048 // 16
+    assert lib.frt_nvfp4_scale_bytes(1, 64) == 128 * 4
+    assert lib.frt_nvfp4_scale_bytes(200, 512) == 256 * 32
+    assert lib.frt_nvfp4_scale_bytes(0, 64) == 0
+    assert lib.frt_nvfp4_scale_bytes(16, 96) == 0  # K not a multiple of 64
+    assert lib.frt_quantize_nvfp4_workspace_bytes() == 16
+    assert lib.frt_gemm_next_scale_workspace_bytes() == 256
+
+
+def test_nvfp4_quantize_rejects_bad_arguments(lib):
+    code = {name: c for c, name in _lib.STATUS_NAMES.items()}
+    sfb = lib.frt_nvfp4_scale_bytes(64, 256)
+    names = ["x", "dt", "rows", "cols", "ldx", "along", "static", "q", "sf", "sfb", "scale", "ws",
+             "wsb", "stream"]
+    ok = [FAKE, _lib.FRT_BF16, 64, 256, 256, 0, None, FAKE, FAKE, sfb, FAKE, FAKE, 16, None]
+
+    def call(**kw):
+        a = list(ok)
+        for k, v in kw.items():
+            a[names.index(k)] = v
+        return lib.frt_quantize_nvfp4(*a)
+
+    for kw, want in ((dict(x=None), "FRT_ERR_INVALID_ARG"), (dict(sf=None), "FRT_ERR_INVALID_ARG"),
+                     (dict(dt=_lib.FRT_E4M3_OCP), "FRT_ERR_INVALID_ARG"),
+                     (dict(rows=0), "FRT_ERR_INVALID_ARG"), (dict(ldx=128), "FRT_ERR_INVALID_ARG"),
+                     (dict(cols=96, ldx=96), "FRT_ERR_UNSUPPORTED_SHAPE"),
+                     (dict(along=1, rows=96), "FRT_ERR_UNSUPPORTED_SHAPE"),  # blocks down 96 rows
+                     (dict(sfb=sfb - 1), "FRT_ERR_WORKSPACE_TOO_SMALL"),
+                     (dict(ws=None), "FRT_ERR_WORKSPACE_TOO_SMALL"),
+                     (dict(wsb=8), "FRT_ERR_WORKSPACE_TOO_SMALL"),
+                     (dict(x=FAKE + 8), "FRT_ERR_MISALIGNED"), (dict(q=FAKE + 4), "FRT_ERR_MISALIGNED"),
+                     (dict(ldx=260), "FRT_ERR_MISALIGNED")):  # 520-byte rows
+        assert call(**kw) == code[want], kw
+
+
+def test_nvfp4_gemm_rejects_bad_arguments(lib):
+    code = {name: c for c, name in _lib.STATUS_NAMES.items()}
+    names = ["a", "lda", "a_sf", "a_scale", "w", "w_sf", "w_scale", "bias", "M", "N", "K", "act",
+             "act_cols", "out", "ldo", "status", "stream"]
+    ok = [FAKE, 128, FAKE, FAKE, FAKE, FAKE, FAKE, None, 64, 256, 256, 0, 0, FAKE, 256, None, None]
+
+    def call(**kw):
+        a = list(ok)
+        for k, v in kw.items():
+            a[names.index(k)] = v
+        return lib.frt_gemm_nvfp4(*a)
+
+    for kw, want in ((dict(a=None), "FRT_ERR_INVALID_ARG"), (dict(w_sf=None), "FRT_ERR_INVALID_ARG"),
+                     (dict(act=_lib.FRT_ACT_GEGLU), "FRT_ERR_INVALID_ARG"),
+                     (dict(act=1, act_cols=512), "FRT_ERR_INVALID_ARG"),
+                     (dict(M=0), "FRT_ERR_INVALID_ARG"), (dict(lda=64), "FRT_ERR_INVALID_ARG"),
+                     (dict(ldo=128), "FRT_ERR_INVALID_ARG"),
+                     (dict(K=192, lda=96), "FRT_ERR_UNSUPPORTED_SHAPE"),
+                     (dict(N=200, ldo=200), "FRT_ERR_UNSUPPORTED_SHAPE"),
+                     (dict(a=FAKE + 8), "FRT_ERR_MISALIGNED"), (dict(lda=136), "FRT_ERR_MISALIGNED"),
+                     (dict(ldo=260), "FRT_ERR_MISALIGNED")):
+        assert call(**kw) == code[want], kw
+
+
+def test_next_scale_gemm_rejects_bad_arguments(lib):
+    code = {name: c for c, name in _lib.STATUS_NAMES.items()}
+    names = ["a", "lda", "a_scale", "w", "w_scale", "bias", "M", "N", "K", "act", "act_cols", "out",
+             "ldo", "scale_cols", "scale", "sws", "swsb", "ws", "wsb", "status", "stream"]
+    ok = [FAKE, 1024, FAKE, FAKE, FAKE, None, 50, 1024, 1024, 0, 0, FAKE, 1024, 1024, FAKE, FAKE,
+          256, None, 0, None, None]
+
+    def call(**kw):
+        a = list(ok)
+        for k, v in kw.items():
+            a[names.index(k)] = v
+        return lib.frt_gemm_fp8_next_scale(*a)
+
+    for kw, want in ((dict(scale=None), "FRT_ERR_INVALID_ARG"), (dict(sws=None), "FRT_ERR_INVALID_ARG"),
+                     (dict(scale_cols=0), "FRT_ERR_INVALID_ARG"),
+                     (dict(scale_cols=2048), "FRT_ERR_INVALID_ARG"),  # past the output's columns
+                     (dict(scale_cols=1020), "FRT_ERR_UNSUPPORTED_SHAPE"),
+                     (dict(scale=FAKE + 2), "FRT_ERR_MISALIGNED"),
+                     (dict(sws=FAKE + 8), "FRT_ERR_MISALIGNED"),
+                     (dict(swsb=128), "FRT_ERR_WORKSPACE_TOO_SMALL")):
+        assert call(**kw) == code[want], kw
+    # the BF16 variant runs the same checks
+    b = lib.frt_gemm_bf16_next_scale
+    assert b(FAKE, 1024, FAKE, None, None, 50, 1024, 1024, 0, 0, FAKE, 1024, 1020, FAKE, FAKE, 256,
+             None, 0, None, None) == code["FRT_ERR_UNSUPPORTED_SHAPE"]
