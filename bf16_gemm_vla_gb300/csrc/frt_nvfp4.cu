@@ -202,6 +202,9 @@ __global__ void __launch_bounds__(kNvQThreads) nvfp4_encode_kernel(
   __syncthreads();
   const float g = g_sh;
   const float d = __fmul_rn(6.0f, g);
+  // RN(1 / d), for the block scales' bracket when it is a positive normal number
+  const float rd = __frcp_rn(d);
+  const bool fast_d = (__float_as_uint(rd) >> 23) - 1u < 254u;
   // (the host keeps vpad * nb below 2^31: 32-bit index arithmetic)
   const uint32_t nb = static_cast<uint32_t>(Kd / kBlk);  // blocks per vector
   const uint32_t vpad = static_cast<uint32_t>((V + 127) / 128 * 128);
@@ -218,7 +221,14 @@ __global__ void __launch_bounds__(kNvQThreads) nvfp4_encode_kernel(
       b = fmaxf(b, fabsf(f[i]));
       nan |= f[i] != f[i];
     }
-    const uint32_t sbyte = encode_e4m3<false>(__fdiv_rn(b, d));  // b >= 0, d > 0: non-negative
+    // sb = E4M3(RN(b / d)) (b >= 0, d > 0: a non-negative byte), by the bracket of
+    // the E4M3 quantize on z = b * RN(1 / d): both ends converted by one hardware
+    // conversion, the IEEE division where their bytes differ
+    const float z = b * rd;
+    const uint32_t c2 = cvt_e4m3x2_ocp(z * (1.0f - 0x1p-20f), z * (1.0f + 0x1p-20f));
+    const uint32_t sbyte = (fast_d && (c2 & 0xFFu) == (c2 >> 8))
+                               ? (c2 & 0xFFu)
+                               : encode_e4m3<false>(__fdiv_rn(b, d));
     const float e = __fmul_rn(e4m3_value_pos(sbyte), g);
     const float r = __frcp_rn(e);
     const bool fast = e > 0.0f && (__float_as_uint(r) >> 23) - 1u < 254u;
@@ -1021,8 +1031,9 @@ frt_status quantize_nvfp4_typed(const T* x, int64_t rows, int64_t cols, int64_t 
   const int64_t V = along_rows ? cols : rows;
   const int64_t Kd = along_rows ? rows : cols;
   const int64_t total = ceil_div(V, 128) * 128 * (Kd / kBlk);
-  cfg.gridDim = dim3(static_cast<unsigned>(
-      std::max<int64_t>(1, std::min<int64_t>(ceil_div(total, kNvQThreads), 8 * sms))));
+  // one block per thread (an uneven share of blocks per thread left most warps
+  // waiting at the end-of-CTA barrier)
+  cfg.gridDim = dim3(static_cast<unsigned>(std::max<int64_t>(1, ceil_div(total, kNvQThreads))));
   if (e == cudaSuccess)
     e = along_rows ? cudaLaunchKernelEx(&cfg, nvfp4_encode_kernel<T, true>, x, V, Kd, ldx,
                                         static_scale, ws, q, sf, scale)
