@@ -458,10 +458,13 @@ __device__ __forceinline__ float grid_scale(float m, unsigned g0, unsigned* hdr,
           break;
         }
         // ... or, once the last arrival has cleared it, the published s
-        const unsigned long long w = ld_relaxed_gpu_u64(hdr + 2);
-        if (static_cast<unsigned>(w) != g0) {
-          sc = __uint_as_float(static_cast<unsigned>(w >> 32));
-          break;
+        // (looked at every fourth poll: the count is the usual signal)
+        if ((it & 3u) == 3u) {
+          const unsigned long long w = ld_relaxed_gpu_u64(hdr + 2);
+          if (static_cast<unsigned>(w) != g0) {
+            sc = __uint_as_float(static_cast<unsigned>(w >> 32));
+            break;
+          }
         }
         if ((it & 15u) == 15u && dev::globaltimer_ns() - t0 > dev::kWaitLimitNs) {
           fail = true;
